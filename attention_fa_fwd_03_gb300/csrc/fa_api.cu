@@ -1,0 +1,295 @@
+// C ABI of the attention library: argument validation, TMA map encoding and
+// dispatch to the per-head-dim kernels. Nothing here allocates device memory.
+//
+// The checks follow the conventions of include/fa.h: errors are returned
+// before anything is launched and never abort the process (page
+// "R/ag_flash_attn.R" (ggmlR), the f32-only backward note: an abort inside the
+// library took the whole session down, so every shape error is reported to
+// the caller instead).
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/fa.h"
+#include "fa_launch.h"
+
+namespace fa {
+
+__device__ uint32_t g_device_status;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+uint64_t wait_timeout_ns() {
+  static const uint64_t ns = [] {
+    const char* env = std::getenv("FA_WAIT_TIMEOUT_MS");
+    long ms = env ? std::strtol(env, nullptr, 10) : 0;
+    if (ms <= 0) ms = 4000;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+  }();
+  return ns;
+}
+
+bool status_ptr(uint32_t** p) {
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return false;
+  *p = static_cast<uint32_t*>(addr);
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// [lo, hi) byte ranges of two buffers intersect.
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+constexpr int kMaxSeq = 1 << 22;        // keeps every grid dimension within limits
+constexpr int64_t kMaxHeads = 1 << 24;  // B * Hq
+
+fa_status check_common(int B, int Hq, int Hkv, int Tq, int Tkv, int D, float scale, int causal,
+                       int window, fa_dtype dt) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tkv < 1) return FA_ERR_INVALID_ARG;
+  if (Tq > kMaxSeq || Tkv > kMaxSeq) return FA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * Hq > kMaxHeads) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!(D == 64 || D == 96 || D == 128 || D == 256)) return FA_ERR_UNSUPPORTED_HEAD_DIM;
+  if (dt != FA_FP16 && dt != FA_BF16) return FA_ERR_UNSUPPORTED_DTYPE;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (window < 0) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+AttnShape make_shape(int B, int Hq, int Hkv, int Tq, int Tkv, int causal, int window,
+                     float scale) {
+  AttnShape s;
+  s.B = B; s.Hq = Hq; s.Hkv = Hkv; s.Tq = Tq; s.Tkv = Tkv;
+  s.causal = causal; s.window = window;
+  s.scale_log2 = scale * kLog2e;
+  return s;
+}
+
+}  // namespace
+
+bool encode_tile_map(CUtensorMap* map, const void* base, bool bf16, int D, int T, int BH,
+                     int box_rows) {
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(D) * 2 * static_cast<cuuint64_t>(T)};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                              3, const_cast<void*>(base), dims, strides, box, elem_strides,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 1;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_abi_version(void) { return 100; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED_HEAD_DIM: return "unsupported head dim (64, 96, 128, 256)";
+    case FA_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype (fp16, bf16)";
+    case FA_ERR_MISALIGNED: return "buffer not 16-byte aligned";
+    case FA_ERR_LAUNCH: return "CUDA launch or driver call failed";
+    case FA_ERR_TIMEOUT: return "a bounded device wait gave up";
+  }
+  return "unknown status";
+}
+
+size_t fa_bwd_workspace_size(int B, int Hq, int Tq) {
+  if (B < 1 || Hq < 1 || Tq < 1) return 0;
+  const size_t bytes = static_cast<size_t>(B) * Hq * Tq * sizeof(float);
+  return (bytes + 255) / 256 * 256;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int Tq, int Tkv, int D, float scale, int causal, int window,
+                 fa_dtype dt, cudaStream_t stream) {
+  fa_status st = check_common(B, Hq, Hkv, Tq, Tkv, D, scale, causal, window, dt);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  const size_t nq = static_cast<size_t>(B) * Hq * Tq * D * 2;
+  const size_t nkv = static_cast<size_t>(B) * Hkv * Tkv * D * 2;
+  const size_t nl = static_cast<size_t>(B) * Hq * Tq * 4;
+  if (overlap(o, nq, q, nq) || overlap(o, nq, k, nkv) || overlap(o, nq, v, nkv) ||
+      overlap(lse, nl, q, nq) || overlap(lse, nl, k, nkv) || overlap(lse, nl, v, nkv) ||
+      overlap(lse, nl, o, nq))
+    return FA_ERR_INVALID_ARG;
+  FwdLaunch a;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.s = make_shape(B, Hq, Hkv, Tq, Tkv, causal, window, scale);
+  a.bf16 = dt == FA_BF16;
+  if (!status_ptr(&a.wc.status)) return FA_ERR_LAUNCH;
+  a.wc.timeout_ns = wait_timeout_ns();
+  a.stream = stream;
+  cudaError_t e;
+  switch (D) {
+    case 64: e = launch_fwd_d64(a); break;
+    case 96: e = launch_fwd_d96(a); break;
+    case 128: e = launch_fwd_d128(a); break;
+    default: e = launch_fwd_d256(a); break;
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared path of fa_bwd and its three phase calls. Pointers a phase does not
+// read or write may be null; everything it does use is checked.
+fa_status bwd_common(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                     int Tq, int Tkv, int D, float scale, int causal, int window, fa_dtype dt,
+                     void* dvec, size_t dvec_bytes, cudaStream_t stream, int phases) {
+  fa_status st = check_common(B, Hq, Hkv, Tq, Tkv, D, scale, causal, window, dt);
+  if (st != FA_OK) return st;
+  const bool pre = phases & kPhaseDvec, dkv = phases & kPhaseDkv, dqp = phases & kPhaseDq;
+  const bool need_qkv = dkv || dqp;
+  if (!dO || !dvec) return FA_ERR_INVALID_ARG;
+  if (pre && !o) return FA_ERR_INVALID_ARG;
+  if (need_qkv && (!q || !k || !v || !lse)) return FA_ERR_INVALID_ARG;
+  if (dkv && (!dk || !dv)) return FA_ERR_INVALID_ARG;
+  if (dqp && !dq) return FA_ERR_INVALID_ARG;
+  if (dvec_bytes < fa_bwd_workspace_size(B, Hq, Tq)) return FA_ERR_INVALID_ARG;
+  const void* all[10] = {q, k, v, o, dO, lse, dq, dk, dv, dvec};
+  for (const void* p : all)
+    if (p && !aligned16(p)) return FA_ERR_MISALIGNED;
+  const size_t nq = static_cast<size_t>(B) * Hq * Tq * D * 2;
+  const size_t nkv = static_cast<size_t>(B) * Hkv * Tkv * D * 2;
+  const size_t nl = static_cast<size_t>(B) * Hq * Tq * 4;
+  // outputs of the requested phases (the D-vector is an output of pass 1 and
+  // an input of passes 2-3)
+  const void* ins[6] = {q, k, v, o, dO, lse};
+  const size_t in_n[6] = {nq, nkv, nkv, nq, nq, nl};
+  const void* outs[4] = {dqp ? dq : nullptr, dkv ? dk : nullptr, dkv ? dv : nullptr, dvec};
+  const size_t out_n[4] = {nq, nkv, nkv, dvec_bytes};
+  for (int i = 0; i < 4; ++i) {
+    if (!outs[i]) continue;
+    for (int j = 0; j < 6; ++j)
+      if (ins[j] && overlap(outs[i], out_n[i], ins[j], in_n[j])) return FA_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 4; ++j)
+      if (outs[j] && overlap(outs[i], out_n[i], outs[j], out_n[j])) return FA_ERR_INVALID_ARG;
+  }
+  BwdLaunch a;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dO; a.lse = lse;
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  a.dvec = static_cast<float*>(dvec);
+  a.scale = scale;
+  a.s = make_shape(B, Hq, Hkv, Tq, Tkv, causal, window, scale);
+  a.bf16 = dt == FA_BF16;
+  if (!status_ptr(&a.wc.status)) return FA_ERR_LAUNCH;
+  a.wc.timeout_ns = wait_timeout_ns();
+  a.stream = stream;
+  cudaError_t e;
+  switch (D) {
+    case 64: e = launch_bwd_d64(a, phases); break;
+    case 96: e = launch_bwd_d96(a, phases); break;
+    case 128: e = launch_bwd_d128(a, phases); break;
+    default: e = launch_bwd_d256(a, phases); break;
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Tq,
+                 int Tkv, int D, float scale, int causal, int window, fa_dtype dt,
+                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace) {
+    // keep the shape errors first, as for every entry point
+    fa_status st = check_common(B, Hq, Hkv, Tq, Tkv, D, scale, causal, window, dt);
+    return st != FA_OK ? st : FA_ERR_INVALID_ARG;
+  }
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Tq, Tkv, D, scale, causal,
+                    window, dt, workspace, workspace_bytes, stream, kPhaseAll);
+}
+
+fa_status fa_bwd_preprocess(const void* o, const void* dO, float* dvec, int B, int Hq, int Tq,
+                            int D, fa_dtype dt, cudaStream_t stream) {
+  // the D-vector does not depend on the mask, scale or KV shape
+  return bwd_common(nullptr, nullptr, nullptr, o, dO, nullptr, nullptr, nullptr, nullptr, B, Hq,
+                    Hq, Tq, 1, D, 1.f, 0, 0, dt, dvec, fa_bwd_workspace_size(B, Hq, Tq), stream,
+                    kPhaseDvec);
+}
+
+fa_status fa_bwd_dkv(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, const float* dvec, void* dk, void* dv, int B, int Hq,
+                     int Hkv, int Tq, int Tkv, int D, float scale, int causal, int window,
+                     fa_dtype dt, cudaStream_t stream) {
+  return bwd_common(q, k, v, nullptr, dO, lse, nullptr, dk, dv, B, Hq, Hkv, Tq, Tkv, D, scale,
+                    causal, window, dt, const_cast<float*>(dvec),
+                    fa_bwd_workspace_size(B, Hq, Tq), stream, kPhaseDkv);
+}
+
+fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
+                    const float* lse, const float* dvec, void* dq, int B, int Hq, int Hkv,
+                    int Tq, int Tkv, int D, float scale, int causal, int window, fa_dtype dt,
+                    cudaStream_t stream) {
+  return bwd_common(q, k, v, nullptr, dO, lse, dq, nullptr, nullptr, B, Hq, Hkv, Tq, Tkv, D,
+                    scale, causal, window, dt, const_cast<float*>(dvec),
+                    fa_bwd_workspace_size(B, Hq, Tq), stream, kPhaseDq);
+}
+
+fa_status fa_device_status(unsigned int* bits, int clear, cudaStream_t stream) {
+  if (!bits) return FA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v)) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (clear && v != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+  }
+  *bits = v;
+  return v == 0 ? FA_OK : FA_ERR_TIMEOUT;
+}
+
+}  // extern "C"

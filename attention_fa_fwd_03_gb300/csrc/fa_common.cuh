@@ -1,0 +1,70 @@
+// Shared definitions of the attention kernels: launch parameters, the mask
+// predicate, and the tile ranges that causal / sliding-window skipping uses.
+//
+// Mask (page "mlx-bun 0.0.4: package/src/model/flash-attention.ts", forward
+// shader): key j is hidden from query i when (causal && j > i) or
+// (window > 0 && i >= j && i - j >= window). Keys at or beyond Tkv and queries
+// at or beyond Tq (tile padding) are hidden as well.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Rows of the query tile one MMA covers (M of tcgen05.mma, one TMEM lane each).
+constexpr int kBM = 128;
+
+struct AttnShape {
+  int B, Hq, Hkv, Tq, Tkv;
+  int causal, window;
+  float scale_log2;  // scale * log2(e): scores are handled in the exp2 domain
+};
+
+struct WaitCfg {
+  uint32_t* status;    // device status word
+  uint64_t timeout_ns; // bound of every mbarrier wait
+};
+
+__host__ __device__ __forceinline__ bool key_visible(int i, int j, int causal, int window) {
+  if (causal && j > i) return false;
+  if (window > 0 && i >= j && i - j >= window) return false;
+  return true;
+}
+
+// Keys that any query in [q_lo, q_hi) can see: [first, last) (may be empty).
+__host__ __device__ __forceinline__ void key_range(const AttnShape& s, int q_lo, int q_hi,
+                                                   int* first, int* last) {
+  int lo = 0, hi = s.Tkv;
+  if (s.causal) hi = min(hi, q_hi);              // j <= i <= q_hi - 1
+  if (s.window > 0) lo = max(0, q_lo - s.window + 1);
+  *first = lo;
+  *last = max(lo, hi);
+}
+
+// Queries that can see any key in [k_lo, k_hi): [first, last) (may be empty).
+__host__ __device__ __forceinline__ void query_range(const AttnShape& s, int k_lo, int k_hi,
+                                                     int* first, int* last) {
+  int lo = 0, hi = s.Tq;
+  if (s.causal) lo = k_lo;                        // i >= j >= k_lo
+  if (s.window > 0) hi = min(hi, k_hi - 1 + s.window);  // i - j < window
+  *first = min(lo, s.Tq);
+  *last = max(*first, hi);
+}
+
+// True when every (query, key) pair of the block [q_lo, q_hi) x [k_lo, k_hi)
+// is visible and in range, so the block needs no per-element mask.
+__host__ __device__ __forceinline__ bool block_unmasked(const AttnShape& s, int q_lo, int q_hi,
+                                                        int k_lo, int k_hi) {
+  if (q_hi > s.Tq || k_hi > s.Tkv) return false;
+  if (s.causal && k_hi - 1 > q_lo) return false;
+  if (s.window > 0 && (q_hi - 1) - k_lo >= s.window) return false;
+  return true;
+}
+
+}  // namespace fa

@@ -1,0 +1,231 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs, element by element.
+
+Tolerances (the headline requirement for fp16/bf16 inputs): O max-abs error
+<= 2e-2; dQ, dK, dV relative Frobenius error <= 1e-2; LSE absolute error
+<= 1e-3 on finite entries, with -inf exactly where the oracle has -inf.
+
+Small workloads are compared in full (or on whole (batch, KV group) slices,
+which are independent problems). The two large workloads run at full size in
+the same launch configuration the benchmark times; their outputs are compared
+on sampled query-row ranges of one group, where the oracle is exact: O, LSE
+and dQ on every sampled row, and dK/dV on key rows whose visible query rows
+all lie in the sampled range. Properties that hold at any size (no NaN, each
+dK column block sums to zero over keys, dV sums to the group's dO) cover the
+rest of the output.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import fa_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+O_TOL, LSE_TOL, GRAD_TOL = 2e-2, 1e-3, 1e-2
+
+
+def fa():
+    import attention_fa_fwd_03_gb300 as m
+    return m
+
+
+def run_gpu(x, w, window=None):
+    """fwd + bwd on the GPU; returns CPU float64 numpy arrays."""
+    m = fa()
+    window = w.window if window is None else window
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    # poison outputs so that a row the kernels forget to write shows up
+    for t in (o, dq, dk, dv):
+        t.fill_(float("nan"))
+    lse.fill_(float("nan"))
+    ws = torch.empty(m.fa_bwd_workspace_size(*q.shape[:3]), dtype=torch.uint8, device=dev)
+    m.fa_fwd(q, k, v, o, lse, w.scale, w.causal, window)
+    m.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.scale, w.causal, window, workspace=ws)
+    torch.cuda.synchronize()
+    assert m.fa_device_status() == 0, "a bounded device wait gave up"
+    out = {n: t.double().cpu().numpy() for n, t in
+           (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    return out
+
+
+def rel_fro(a, b):
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / nb) if nb > 0 else float(np.linalg.norm(a))
+
+
+def check_fwd(o, lse, ro, rlse, what=""):
+    assert not np.isnan(o).any(), f"{what}: NaN in O"
+    err = np.abs(o - ro).max()
+    assert err <= O_TOL, f"{what}: O max-abs {err:.3e}"
+    assert np.array_equal(np.isneginf(lse), np.isneginf(rlse)), f"{what}: -inf LSE pattern"
+    fin = np.isfinite(rlse)
+    lerr = np.abs(lse[fin] - rlse[fin]).max() if fin.any() else 0.0
+    assert lerr <= LSE_TOL, f"{what}: LSE max-abs {lerr:.3e}"
+    return err, lerr
+
+
+def check_grads(g, r, what="", names=("dq", "dk", "dv")):
+    errs = {}
+    for n in names:
+        assert not np.isnan(g[n]).any(), f"{what}: NaN in {n}"
+        errs[n] = rel_fro(g[n], r[n])
+        assert errs[n] <= GRAD_TOL, f"{what}: {n} rel-Frobenius {errs[n]:.3e}"
+    return errs
+
+
+def as64(x, names=("q", "k", "v", "do")):
+    return [x[n].double().numpy() for n in names]
+
+
+def group_views(x, b, g, reps):
+    h0, h1 = g * reps, (g + 1) * reps
+    return {"q": x["q"][b:b + 1, h0:h1], "k": x["k"][b:b + 1, g:g + 1],
+            "v": x["v"][b:b + 1, g:g + 1], "do": x["do"][b:b + 1, h0:h1]}
+
+
+def compare_full(w, x=None, window=None):
+    x = x or fa_inputs.make_inputs(w)
+    window = w.window if window is None else window
+    got = run_gpu(x, w, window)
+    ref = oracle.attn_bwd(*as64(x), w.scale, w.causal, window)
+    check_fwd(got["o"], got["lse"], ref["o"], ref["lse"], w.name)
+    return check_grads(got, ref, w.name)
+
+
+def compare_groups(w, groups):
+    """Full GPU run; oracle on whole (batch, KV group) slices."""
+    x = fa_inputs.make_inputs(w)
+    got = run_gpu(x, w)
+    reps = w.Hq // w.Hkv
+    for (b, g) in groups:
+        xs = group_views(x, b, g, reps)
+        ref = oracle.attn_bwd(*as64(xs), w.scale, w.causal, w.window)
+        h0, h1 = g * reps, (g + 1) * reps
+        sl = {"o": got["o"][b:b + 1, h0:h1], "lse": got["lse"][b:b + 1, h0:h1],
+              "dq": got["dq"][b:b + 1, h0:h1], "dk": got["dk"][b:b + 1, g:g + 1],
+              "dv": got["dv"][b:b + 1, g:g + 1]}
+        check_fwd(sl["o"], sl["lse"], ref["o"], ref["lse"], f"{w.name} b{b} g{g}")
+        check_grads(sl, ref, f"{w.name} b{b} g{g}")
+    return got, x
+
+
+# ---------------------------------------------------------------- workloads
+def test_c1_smoke_shape_full():
+    compare_full(fa_inputs.WORKLOADS["c1_b1_h2x1_t64_d64_fp16_causal"])
+
+
+def test_c2_mha_noncausal_full():
+    compare_full(fa_inputs.WORKLOADS["c2_b2_h8x8_t1024_d128_bf16"])
+
+
+@pytest.mark.parametrize("name", ["c5a_b2_h8x2_t2048_d64_fp16_causal",
+                                  "c5b_b2_h8x2_t2048_d96_fp16_causal",
+                                  "c5c_b2_h8x2_t2048_d256_fp16_causal",
+                                  "c5d_b2_h8x2_tq512_tkv2048_d128_fp16"])
+def test_c5_shape_sweep_group_slices(name):
+    w = fa_inputs.WORKLOADS[name]
+    compare_groups(w, [(0, 0), (1, w.Hkv - 1)])
+
+
+@pytest.mark.parametrize("name", ["c5e1_b2_h8x2_tq1_tkv1024_d128_fp16",
+                                  "c5e4_b2_h8x2_tq4_tkv1024_d128_fp16",
+                                  "c5e8_b2_h8x2_tq8_tkv1024_d128_fp16"])
+def test_c5e_short_queries_full(name):
+    compare_full(fa_inputs.WORKLOADS[name])
+
+
+def check_large_sampled(w, head_rows=256, tail_rows=256, groups=((0, 0),)):
+    x = fa_inputs.make_inputs(w)
+    got = run_gpu(x, w)
+    reps = w.Hq // w.Hkv
+    for name in ("o", "dq", "dk", "dv"):
+        assert np.isfinite(got[name]).all(), f"non-finite values in {name}"
+    assert np.isfinite(got["lse"]).all()
+    for (b, g) in groups:
+        xs = as64(group_views(x, b, g, reps))
+        h0, h1 = g * reps, (g + 1) * reps
+        # head rows: O, LSE, dQ exact
+        ref = oracle.attn_bwd(*xs, w.scale, w.causal, w.window, row_lo=0, row_hi=head_rows)
+        check_fwd(got["o"][b, h0:h1, :head_rows], got["lse"][b, h0:h1, :head_rows],
+                  ref["o"][0, :, :head_rows], ref["lse"][0, :, :head_rows], f"{w.name} head rows")
+        e = rel_fro(got["dq"][b, h0:h1, :head_rows], ref["dq"][0, :, :head_rows])
+        assert e <= GRAD_TOL, f"dq head rows {e:.3e}"
+        # tail rows: O, LSE, dQ exact; dK/dV exact for keys >= Tq - tail_rows (causal)
+        lo = w.Tq - tail_rows
+        ref = oracle.attn_bwd(*xs, w.scale, w.causal, w.window, row_lo=lo, row_hi=w.Tq)
+        check_fwd(got["o"][b, h0:h1, lo:], got["lse"][b, h0:h1, lo:],
+                  ref["o"][0, :, lo:], ref["lse"][0, :, lo:], f"{w.name} tail rows")
+        for n, gv, rv in (("dq", got["dq"][b, h0:h1, lo:], ref["dq"][0, :, lo:]),
+                          ("dk", got["dk"][b, g, lo:], ref["dk"][0, 0, lo:]),
+                          ("dv", got["dv"][b, g, lo:], ref["dv"][0, 0, lo:])):
+            e = rel_fro(gv, rv)
+            assert e <= GRAD_TOL, f"{w.name} {n} tail rows rel-Frobenius {e:.3e}"
+    # any-size properties: softmax rows sum to one / dS rows sum to zero
+    dk_sum = got["dk"].sum(axis=2)
+    assert np.abs(dk_sum).max() <= 1e-2 * np.abs(got["dk"]).sum(axis=2).max() + 1e-3
+    want_dv = x["do"].double().numpy().reshape(w.B, w.Hkv, reps, w.Tq, w.D).sum(axis=(2, 3))
+    got_dv = got["dv"].sum(axis=2)
+    assert rel_fro(got_dv, want_dv) <= 1e-2
+
+
+def test_c3_headline_full_size_sampled():
+    check_large_sampled(fa_inputs.WORKLOADS["c3_b4_h32x8_t4096_d128_bf16_causal"],
+                        groups=((0, 0), (3, 7)))
+
+
+def test_c4_sliding_window_full_size_sampled():
+    check_large_sampled(fa_inputs.WORKLOADS["c4_b1_h16x2_t16384_d128_bf16_causal_w4096"],
+                        groups=((0, 1),))
+
+
+# --------------------------------------------------------------- edge cases
+EDGE = [
+    # (B, Hq, Hkv, Tq, Tkv, D, dtype, causal, window)
+    (1, 2, 1, 200, 200, 128, "bf16", True, 0),       # ragged tail, several tiles
+    (2, 4, 4, 333, 333, 64, "fp16", False, 0),
+    (1, 4, 2, 129, 129, 96, "bf16", True, 0),
+    (1, 2, 1, 257, 257, 256, "bf16", True, 0),
+    (1, 2, 2, 300, 300, 256, "fp16", False, 0),
+    (1, 16, 1, 150, 150, 64, "bf16", True, 0),       # GQA 16:1
+    (1, 8, 1, 140, 140, 128, "fp16", True, 0),       # GQA 8:1
+    (1, 4, 1, 500, 500, 128, "bf16", True, 100),     # causal window
+    (1, 4, 2, 400, 400, 64, "fp16", False, 77),      # window without causal (future visible)
+    (1, 2, 1, 300, 100, 128, "bf16", True, 40),      # fully masked rows (Tq > Tkv + window)
+    (1, 2, 1, 77, 300, 128, "bf16", True, 0),        # Tq < Tkv causal (top-left)
+    (1, 2, 1, 300, 77, 64, "fp16", True, 0),         # Tq > Tkv causal
+    (2, 4, 2, 1, 257, 128, "bf16", False, 0),        # single query row
+    (1, 2, 1, 1, 1, 64, "fp16", False, 0),           # single key and query
+    (1, 2, 2, 5, 700, 256, "bf16", False, 0),        # short queries, D=256
+    (3, 6, 3, 256, 384, 96, "fp16", False, 0),       # exact tile multiples, cross-attention
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tq,Tkv,D,dt,causal,window", EDGE)
+def test_edge_cases(B, Hq, Hkv, Tq, Tkv, D, dt, causal, window):
+    w = fa_inputs.Workload(f"edge_{B}_{Hq}_{Hkv}_{Tq}_{Tkv}_{D}_{dt}_{int(causal)}_{window}",
+                           B, Hq, Hkv, Tq, Tkv, D, dt, causal, window,
+                           seed=1000 + Tq + 7 * Tkv + D)
+    compare_full(w)
+
+
+def test_large_values_stay_finite():
+    """Sharp softmax (Q, K scaled by 8) exercises the lazy rescale path."""
+    w = fa_inputs.Workload("sharp", 1, 2, 1, 700, 700, 128, "bf16", True, qk_mult=8.0, seed=77)
+    compare_full(w)
+
+
+def test_repeat_calls_are_deterministic():
+    w = fa_inputs.Workload("det", 1, 4, 2, 300, 300, 128, "bf16", True, seed=5)
+    x = fa_inputs.make_inputs(w)
+    a = run_gpu(x, w)
+    b = run_gpu(x, w)
+    for n in a:
+        assert np.array_equal(np.nan_to_num(a[n], neginf=-1e300), np.nan_to_num(b[n], neginf=-1e300)), n
