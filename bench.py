@@ -72,18 +72,30 @@ def load_peaks() -> dict:
             "source": "fallback"}
 
 
-def source_digest() -> str:
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["fa_fwd.cuh"],
+    "fa_bwd_dvec_kernel": ["fa_bwd.cuh"],
+    "fa_bwd_dkv_kernel": ["fa_bwd.cuh"],
+    "fa_bwd_dq_kernel": ["fa_bwd.cuh"],
+}
+COMMON_SOURCES = ["fa_common.cuh", "sm103_ptx.cuh", "fa_inst.cuh", "fa_inst_d64.cu",
+                  "fa_inst_d96.cu", "fa_inst_d128.cu", "fa_inst_d256.cu"]
+
+
+def kernel_digest(kernel: str) -> str:
+    """Digest of the sources that define ``kernel`` (its body, the shared
+    device helpers and the tile configurations)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_fa_fwd_03_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel] + COMMON_SOURCES:
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(name.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -91,7 +103,7 @@ def ncu_traffic(kernel: str, workload: str):
         rec = json.load(fh)
     for r in rec.get("kernels", []):
         if (r.get("kernel") == kernel and r.get("workload") == workload
-                and r.get("source_digest") == source_digest()):
+                and r.get("source_digest") == kernel_digest(kernel)):
             return r.get("dram_bytes_per_launch")
     return None
 
