@@ -293,3 +293,65 @@ fa_status fa_device_status(unsigned int* bits, int clear, cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// fa_bwd_noalloc: the backward pass for callers that cannot allocate device
+// memory at all, not even the small D-vector workspace fa_bwd asks for — for
+// example a plug-in running inside a host program that owns every device
+// allocation, or a loop that must not call the allocator (which may
+// synchronise the device) once it is running. The D-vector lives instead in
+// the fixed array below, which every device that loads this library keeps
+// until the process exits.
+namespace {
+
+// Largest B * Hq * Tq the array holds: 2^20 fp32 values (4 MiB).
+constexpr size_t kNoallocMaxRows = size_t(1) << 20;
+
+// Device addresses of the array, found once per device (with that device
+// current) on the first fa_bwd_noalloc call made there.
+std::mutex g_noalloc_mutex;
+float* g_noalloc_ptr[64] = {nullptr};
+
+}  // namespace
+
+static __device__ __align__(256) float g_noalloc_scratch[kNoallocMaxRows];
+
+namespace {
+
+fa_status noalloc_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FA_ERR_LAUNCH;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_bwd_noalloc_max_rows(void) { return kNoallocMaxRows; }
+
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int Hq, int Hkv, int Tq, int Tkv, int D, float scale, int causal,
+                         int window, fa_dtype dt, cudaStream_t stream) {
+  fa_status st = check_common(B, Hq, Hkv, Tq, Tkv, D, scale, causal, window, dt);
+  if (st != FA_OK) return st;
+  if (static_cast<size_t>(B) * Hq * Tq > kNoallocMaxRows) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  float* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != FA_OK) return st;
+  // The D-vector is fully rewritten by the first launch of every call, so
+  // nothing in the array has to start at zero.
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Tq, Tkv, D, scale, causal,
+                    window, dt, scratch, kNoallocMaxRows * sizeof(float), stream, kPhaseAll);
+}
+
+}  // extern "C"

@@ -127,6 +127,30 @@ fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
                     int B, int Hq, int Hkv, int Tq, int Tkv, int D, float scale,
                     int causal, int window, fa_dtype dt, cudaStream_t stream);
 
+/* fa_bwd without a workspace argument, for callers that cannot allocate any
+ * device memory: a plug-in inside a host program that owns every device
+ * allocation, or a loop that may not call the allocator (which can
+ * synchronise the device) once it runs. The pages have no counterpart of
+ * this call; it exists for such callers only.
+ * The D-vector goes to a fixed 4 MiB array inside the library instead of a
+ * caller buffer: B * Hq * Tq must not exceed fa_bwd_noalloc_max_rows()
+ * (2^20), else FA_ERR_INVALID_ARG and nothing is launched. Every other
+ * argument, layout and error rule is that of fa_bwd.
+ * The array is one per device, shared by every call on that device and kept
+ * until the process exits; it holds the last call's D-vector. Calls whose
+ * launches overlap on the GPU (two streams, or two host threads) race on it:
+ * keep them ordered on one stream. The first call on a device looks up the
+ * array's device address (with that device current); make that first call
+ * before any stream capture. Nothing in the array has to start at zero: each
+ * call rewrites the part it uses before reading it. */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                         int B, int Hq, int Hkv, int Tq, int Tkv, int D, float scale,
+                         int causal, int window, fa_dtype dt, cudaStream_t stream);
+
+/* Largest B * Hq * Tq that fa_bwd_noalloc accepts. */
+size_t fa_bwd_noalloc_max_rows(void);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* fa_status_string(fa_status s);
 
