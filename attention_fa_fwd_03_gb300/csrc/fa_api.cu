@@ -70,6 +70,10 @@ fa_status check_common(int B, int Hq, int Hkv, int Tq, int Tkv, int D, float sca
   if (Tq > kMaxSeq || Tkv > kMaxSeq) return FA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * Hq > kMaxHeads) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  // every kernel runs a 1-D grid of (head or group) x (128-row block) CTAs
+  if (static_cast<int64_t>(B) * Hq * ((Tq + 127) / 128) > INT32_MAX ||
+      static_cast<int64_t>(B) * Hkv * ((Tkv + 127) / 128) > INT32_MAX)
+    return FA_ERR_INVALID_ARG;
   if (!(D == 64 || D == 96 || D == 128 || D == 256)) return FA_ERR_UNSUPPORTED_HEAD_DIM;
   if (dt != FA_FP16 && dt != FA_BF16) return FA_ERR_UNSUPPORTED_DTYPE;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;

@@ -5,8 +5,8 @@
 //   pass 1  D_i = rowsum(dO_i o O_i) from the stored O           (fa_bwd_dvec_kernel)
 //   pass 2  per KV row block, over every query head of its group and every
 //           query tile: p = exp(s - L), dp = dO.v, ds = p (dp - D),
-//           dV += p dO, dK += ds q scale                          (fa_bwd_dkv_kernel)
-//   pass 3  per query row block, over key tiles: dQ += ds k scale (fa_bwd_dq_kernel)
+//           dV += p dO, dK += ds q scale                          (fa_bwd_dkv_split_kernel)
+//   pass 3  per query row block, over key tiles: dQ += ds k scale (fa_bwd_dq_serial_kernel)
 // and page "[Metal] Add Flash Attention VJP for training", Implementation
 // Notes: two kernels instead of atomics, with the dK/dV kernel owning its KV
 // rows so the query heads of a GQA group are summed without races; the exp2
@@ -65,7 +65,7 @@ fa_bwd_dvec_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
 enum : int { kModeDV = 1, kModeDK = 2 };
 
 template <int D_, int BMQ_, int STAGES_, bool BF16_, int MODE_>
-struct DkvCfg {
+struct DkvSplitCfg {
   static constexpr int D = D_;
   static constexpr int BMQ = BMQ_;   // query rows per inner tile (N of S^T)
   static constexpr int STAGES = STAGES_;
@@ -101,11 +101,11 @@ struct DkvCfg {
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
-fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+fa_bwd_dkv_split_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const float* __restrict__ lse, const float* __restrict__ dvec,
                   void* __restrict__ dk_out, void* __restrict__ dv_out, float scale, AttnShape s,
-                  WaitCfg wc) {
+                  TileOrder order, WaitCfg wc) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -119,10 +119,11 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   float* stats = reinterpret_cast<float*>(smem + C::OFF_STATS);  // [buf][lse2|dvec][BMQ]
 
-  const int bg = blockIdx.x;  // b * Hkv + g
+  int bg, kvt;  // (b * Hkv + g, block of 128 KV rows)
+  decode_tile(blockIdx.x, order, &bg, &kvt);
   const int b = bg / s.Hkv, g = bg % s.Hkv;
   const int reps = s.Hq / s.Hkv;
-  const int k0 = blockIdx.y * kBM;
+  const int k0 = kvt * kBM;
   int qf, ql;
   query_range(s, k0, min(s.Tkv, k0 + kBM), &qf, &ql);
   const int i_lo = qf / C::BMQ;
@@ -325,7 +326,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
 // ------------------------------------------------------------------ pass 3: dQ
 template <int D_, int BN_, int STAGES_, bool BF16_>
-struct DqCfg {
+struct DqSerialCfg {
   static constexpr int D = D_;
   static constexpr int BN = BN_;
   static constexpr int STAGES = STAGES_;
@@ -355,10 +356,11 @@ struct DqCfg {
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
-fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+fa_bwd_dq_serial_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                  const float* __restrict__ lse, const float* __restrict__ dvec,
-                 void* __restrict__ dq_out, float scale, AttnShape s, WaitCfg wc) {
+                 void* __restrict__ dq_out, float scale, AttnShape s, TileOrder order,
+                 WaitCfg wc) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -371,10 +373,11 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
-  const int bh = blockIdx.x;
+  int bh, qt;  // (b * Hq + h, block of 128 query rows)
+  decode_tile(blockIdx.x, order, &bh, &qt);
   const int b = bh / s.Hq, h = bh % s.Hq;
   const int g = h / (s.Hq / s.Hkv);
-  const int q0 = (gridDim.y - 1 - blockIdx.y) * kBM;
+  const int q0 = qt * kBM;
   int kf, kl;
   key_range(s, q0, min(s.Tq, q0 + kBM), &kf, &kl);
   const int j_lo = kf / C::BN;

@@ -31,6 +31,27 @@ struct WaitCfg {
   uint64_t timeout_ns; // bound of every mbarrier wait
 };
 
+// Order in which a 1-D grid visits (unit, tile) work items. A unit is a
+// (batch, head) or (batch, KV group) whose tiles share an operand (K/V, or
+// Q/dO); a tile is a row block. Blocks are dispatched roughly in linear order,
+// so the grid walks `chunk` units at a time (their shared operands then stay
+// resident in L2) and, inside a chunk, the heaviest tiles first (causal
+// masking makes the work per tile uneven), round-robin over the units.
+struct TileOrder {
+  int units, tiles, chunk;
+  int heavy_last;  // 1: the last tile index carries the most work
+};
+
+__device__ __forceinline__ void decode_tile(int linear, const TileOrder& o, int* unit, int* tile) {
+  const int per_chunk = o.chunk * o.tiles;
+  const int c = linear / per_chunk;
+  const int r = linear - c * per_chunk;
+  const int cu = min(o.chunk, o.units - c * o.chunk);  // units in this (maybe last) chunk
+  const int t = r / cu;
+  *unit = c * o.chunk + (r - t * cu);
+  *tile = o.heavy_last ? o.tiles - 1 - t : t;
+}
+
 __host__ __device__ __forceinline__ bool key_visible(int i, int j, int causal, int window) {
   if (causal && j > i) return false;
   if (window > 0 && i >= j && i - j >= window) return false;

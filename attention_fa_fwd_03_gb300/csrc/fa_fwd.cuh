@@ -68,7 +68,7 @@ template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, void* __restrict__ o_out,
-              float* __restrict__ lse_out, AttnShape s, WaitCfg wc) {
+              float* __restrict__ lse_out, AttnShape s, TileOrder order, WaitCfg wc) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -83,12 +83,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
-  // ---- work item: heads fastest so the first wave holds every head's
-  // heaviest (last, under causal masking) query block.
-  const int bh = blockIdx.x;
+  // ---- work item: a (batch, head) and a block of NQ*128 query rows
+  int bh, qblk;
+  decode_tile(blockIdx.x, order, &bh, &qblk);
   const int b = bh / s.Hq, h = bh % s.Hq;
   const int g = h / (s.Hq / s.Hkv);
-  const int qblk = gridDim.y - 1 - blockIdx.y;
   const int q0 = qblk * (C::NQ * kBM);
   int k_first, k_last;
   key_range(s, q0, min(s.Tq, q0 + C::NQ * kBM), &k_first, &k_last);

@@ -4,10 +4,45 @@
 #pragma once
 
 #include "fa_bwd.cuh"
+#include "fa_bwd_pipelined.cuh"
 #include "fa_fwd.cuh"
 #include "fa_launch.h"
 
 namespace fa {
+
+// Units per chunk so that the operands the units' tiles share stay in L2:
+// about 32 MiB of them at a time (the L2 holds 126 MiB, and the streamed
+// per-tile operands and outputs pass through it too), rounded to a multiple
+// of `align` units.
+inline TileOrder make_order(int units, int tiles, int64_t shared_bytes_per_unit, int align,
+                            bool heavy_last) {
+  const int64_t target = int64_t(32) << 20;
+  int64_t chunk = target / (shared_bytes_per_unit > 0 ? shared_bytes_per_unit : 1);
+  chunk = chunk / align * align;
+  if (chunk < align) chunk = align;
+  if (chunk > units) chunk = units;
+  TileOrder o;
+  o.units = units;
+  o.tiles = tiles;
+  o.chunk = static_cast<int>(chunk);
+  o.heavy_last = heavy_last ? 1 : 0;
+  return o;
+}
+
+// Query-row blocks of one head share the group's K and V (reps heads each).
+inline TileOrder query_block_order(const AttnShape& s, int rows_per_block, int D) {
+  const int reps = s.Hq / s.Hkv;
+  const int64_t kv_bytes = int64_t(s.Tkv) * D * 2 * 2;
+  return make_order(s.B * s.Hq, (s.Tq + rows_per_block - 1) / rows_per_block, kv_bytes / reps,
+                    reps, s.causal != 0);
+}
+
+// KV-row blocks of one group share its reps heads' Q and dO.
+inline TileOrder kv_block_order(const AttnShape& s, int D) {
+  const int reps = s.Hq / s.Hkv;
+  const int64_t qdo_bytes = int64_t(reps) * s.Tq * D * 2 * 2;
+  return make_order(s.B * s.Hkv, (s.Tkv + kBM - 1) / kBM, qdo_bytes, 1, false);
+}
 
 template <class C>
 cudaError_t run_fwd(const FwdLaunch& a) {
@@ -21,8 +56,9 @@ cudaError_t run_fwd(const FwdLaunch& a) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const dim3 grid(bhq, (a.s.Tq + C::NQ * kBM - 1) / (C::NQ * kBM));
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, a.o, a.lse, a.s, a.wc);
+  const TileOrder order = query_block_order(a.s, C::NQ * kBM, C::D);
+  kern<<<order.units * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, a.o, a.lse,
+                                                                           a.s, order, a.wc);
   return cudaGetLastError();
 }
 
@@ -40,8 +76,8 @@ cudaError_t run_dvec(const BwdLaunch& a) {
   return cudaGetLastError();
 }
 
-template <class C>
-cudaError_t run_dkv(const BwdLaunch& a) {
+template <class C, class Kern>
+cudaError_t launch_dkv_with(const BwdLaunch& a, Kern kern) {
   const int bhq = a.s.B * a.s.Hq, bhkv = a.s.B * a.s.Hkv;
   CUtensorMap mq, mk, mv, mdo;
   if (!encode_tile_map(&mq, a.q, C::BF16, C::D, a.s.Tq, bhq, C::BMQ) ||
@@ -49,18 +85,17 @@ cudaError_t run_dkv(const BwdLaunch& a) {
       !encode_tile_map(&mk, a.k, C::BF16, C::D, a.s.Tkv, bhkv, kBM) ||
       !encode_tile_map(&mv, a.v, C::BF16, C::D, a.s.Tkv, bhkv, kBM))
     return cudaErrorInvalidValue;
-  auto kern = fa_bwd_dkv_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const dim3 grid(bhkv, (a.s.Tkv + kBM - 1) / kBM);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, mdo, a.lse, a.dvec, a.dk, a.dv,
-                                                       a.scale, a.s, a.wc);
+  const TileOrder order = kv_block_order(a.s, C::D);
+  kern<<<order.units * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream>>>(
+      mq, mk, mv, mdo, a.lse, a.dvec, a.dk, a.dv, a.scale, a.s, order, a.wc);
   return cudaGetLastError();
 }
 
-template <class C>
-cudaError_t run_dq(const BwdLaunch& a) {
+template <class C, class Kern>
+cudaError_t launch_dq_with(const BwdLaunch& a, Kern kern) {
   const int bhq = a.s.B * a.s.Hq, bhkv = a.s.B * a.s.Hkv;
   CUtensorMap mq, mk, mv, mdo;
   if (!encode_tile_map(&mq, a.q, C::BF16, C::D, a.s.Tq, bhq, kBM) ||
@@ -68,48 +103,61 @@ cudaError_t run_dq(const BwdLaunch& a) {
       !encode_tile_map(&mk, a.k, C::BF16, C::D, a.s.Tkv, bhkv, C::BN) ||
       !encode_tile_map(&mv, a.v, C::BF16, C::D, a.s.Tkv, bhkv, C::BN))
     return cudaErrorInvalidValue;
-  auto kern = fa_bwd_dq_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const dim3 grid(bhq, (a.s.Tq + kBM - 1) / kBM);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, mdo, a.lse, a.dvec, a.dq,
-                                                       a.scale, a.s, a.wc);
+  const TileOrder order = query_block_order(a.s, kBM, C::D);
+  kern<<<order.units * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream>>>(
+      mq, mk, mv, mdo, a.lse, a.dvec, a.dq, a.scale, a.s, order, a.wc);
   return cudaGetLastError();
+}
+
+// Backward for one head dim. D <= 128: the pipelined 128 x 128 kernels
+// (fa_bwd_pipelined.cuh) with KST / QST stages. D = 256: the accumulators
+// alone fill TMEM, so dV and dK run as two passes with 64-row query tiles and
+// dQ with 64-column key tiles, one stage (fa_bwd.cuh).
+template <int D, bool BF16, int KST, int QST>
+cudaError_t run_bwd(const BwdLaunch& a, int phases) {
+  cudaError_t e = cudaSuccess;
+  if (phases & kPhaseDvec) e = run_dvec<D, BF16>(a);
+  if (e != cudaSuccess) return e;
+  if (phases & kPhaseDkv) {
+    if constexpr (D <= 128) {
+      using C = DkvCfg<D, KST, BF16>;
+      e = launch_dkv_with<C>(a, fa_bwd_dkv_kernel<C>);
+    } else {
+      using CV = DkvSplitCfg<D, 64, 2, BF16, kModeDV>;
+      using CK = DkvSplitCfg<D, 64, 1, BF16, kModeDK>;
+      e = launch_dkv_with<CV>(a, fa_bwd_dkv_split_kernel<CV>);
+      if (e == cudaSuccess) e = launch_dkv_with<CK>(a, fa_bwd_dkv_split_kernel<CK>);
+    }
+  }
+  if (e != cudaSuccess) return e;
+  if (phases & kPhaseDq) {
+    if constexpr (D <= 128) {
+      using C = DqCfg<D, QST, BF16>;
+      e = launch_dq_with<C>(a, fa_bwd_dq_kernel<C>);
+    } else {
+      using C = DqSerialCfg<D, 64, 1, BF16>;
+      e = launch_dq_with<C>(a, fa_bwd_dq_serial_kernel<C>);
+    }
+  }
+  return e;
 }
 
 }  // namespace fa
 
-// Define launch_fwd_d<D> / launch_bwd_d<D> for one head dim from its tile
-// configurations: forward (NQ, BN, STAGES), dK/dV (query tile, STAGES, and
-// whether dV and dK share one pass), dQ (BN, STAGES).
-#define FA_DEFINE_HEAD_DIM(D, FNQ, FBN, FST, KBMQ, KST_DV, KST_DK, KJOINT, QBN, QST)        \
-  namespace fa {                                                                            \
-  template <bool BF16>                                                                      \
-  static cudaError_t fwd_##D(const FwdLaunch& a) {                                          \
-    return run_fwd<FwdCfg<D, FNQ, FBN, FST, BF16>>(a);                                      \
-  }                                                                                         \
-  template <bool BF16>                                                                      \
-  static cudaError_t bwd_##D(const BwdLaunch& a, int phases) {                              \
-    cudaError_t e = cudaSuccess;                                                            \
-    if (phases & kPhaseDvec) e = run_dvec<D, BF16>(a);                                      \
-    if (e != cudaSuccess) return e;                                                         \
-    if (phases & kPhaseDkv) {                                                               \
-      if constexpr (KJOINT) {                                                               \
-        e = run_dkv<DkvCfg<D, KBMQ, KST_DV, BF16, kModeDV | kModeDK>>(a);                   \
-      } else {                                                                              \
-        e = run_dkv<DkvCfg<D, KBMQ, KST_DV, BF16, kModeDV>>(a);                             \
-        if (e == cudaSuccess) e = run_dkv<DkvCfg<D, KBMQ, KST_DK, BF16, kModeDK>>(a);       \
-      }                                                                                     \
-    }                                                                                       \
-    if (e != cudaSuccess) return e;                                                         \
-    if (phases & kPhaseDq) e = run_dq<DqCfg<D, QBN, QST, BF16>>(a);                         \
-    return e;                                                                               \
-  }                                                                                         \
-  cudaError_t launch_fwd_d##D(const FwdLaunch& a) {                                         \
-    return a.bf16 ? fwd_##D<true>(a) : fwd_##D<false>(a);                                   \
-  }                                                                                         \
-  cudaError_t launch_bwd_d##D(const BwdLaunch& a, int phases) {                             \
-    return a.bf16 ? bwd_##D<true>(a, phases) : bwd_##D<false>(a, phases);                   \
-  }                                                                                         \
+// Define launch_fwd_d<D> / launch_bwd_d<D> for one head dim: forward tile
+// configuration (NQ query tiles per CTA, key tile BN, STAGES), and the stage
+// counts of the pipelined dK/dV and dQ kernels.
+#define FA_DEFINE_HEAD_DIM(D, FNQ, FBN, FST, KST, QST)                                    \
+  namespace fa {                                                                          \
+  cudaError_t launch_fwd_d##D(const FwdLaunch& a) {                                       \
+    return a.bf16 ? run_fwd<FwdCfg<D, FNQ, FBN, FST, true>>(a)                            \
+                  : run_fwd<FwdCfg<D, FNQ, FBN, FST, false>>(a);                          \
+  }                                                                                       \
+  cudaError_t launch_bwd_d##D(const BwdLaunch& a, int phases) {                           \
+    return a.bf16 ? run_bwd<D, true, KST, QST>(a, phases)                                 \
+                  : run_bwd<D, false, KST, QST>(a, phases);                               \
+  }                                                                                       \
   }

@@ -1,8 +1,6 @@
-// Kernels for head dim 128. Tile configuration (chosen for the 227 KB of shared
-// memory and 512 TMEM columns of one SM):
-//   forward: 2 query tile(s) of 128 rows per CTA, key tiles of 128, 2-stage K/V ring
-//   dK/dV:   query tiles of 128 rows, 2-stage Q/dO ring, dV and dK in one pass
-//   dQ:      key tiles of 128, 2-stage K/V ring
+// Kernels for head dim 128:
+//   forward: two 128-row query tiles per CTA, 128-key tiles, 2-stage K/V ring
+//   dK/dV:   128 x 128 tiles, 2-stage Q/dO ring;  dQ: 128 x 128 tiles, 2-stage K/V ring
 #include "fa_inst.cuh"
 
-FA_DEFINE_HEAD_DIM(128, 2, 128, 2, 128, 2, 2, 1, 128, 2)
+FA_DEFINE_HEAD_DIM(128, 2, 128, 2, 2, 2)
