@@ -36,14 +36,17 @@ void load_encode() {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 }
 
-uint64_t wait_timeout_ns() {
-  static const uint64_t ns = [] {
+// Bound of every device wait, in SM clock cycles: FA_WAIT_TIMEOUT_MS (default
+// 4000 ms) at 2.2 GHz, above the GB300's highest SM clock, so at any real
+// clock the wait lasts at least that long.
+uint64_t wait_timeout_cycles() {
+  static const uint64_t cycles = [] {
     const char* env = std::getenv("FA_WAIT_TIMEOUT_MS");
     long ms = env ? std::strtol(env, nullptr, 10) : 0;
     if (ms <= 0) ms = 4000;
-    return static_cast<uint64_t>(ms) * 1000000ull;
+    return static_cast<uint64_t>(ms) * 2200000ull;
   }();
-  return ns;
+  return cycles;
 }
 
 bool status_ptr(uint32_t** p) {
@@ -168,7 +171,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   a.s = make_shape(B, Hq, Hkv, Tq, Tkv, causal, window, scale);
   a.bf16 = dt == FA_BF16;
   if (!status_ptr(&a.wc.status)) return FA_ERR_LAUNCH;
-  a.wc.timeout_ns = wait_timeout_ns();
+  a.wc.timeout_cycles = wait_timeout_cycles();
   a.stream = stream;
   cudaError_t e;
   switch (D) {
@@ -227,7 +230,7 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   a.s = make_shape(B, Hq, Hkv, Tq, Tkv, causal, window, scale);
   a.bf16 = dt == FA_BF16;
   if (!status_ptr(&a.wc.status)) return FA_ERR_LAUNCH;
-  a.wc.timeout_ns = wait_timeout_ns();
+  a.wc.timeout_cycles = wait_timeout_cycles();
   a.stream = stream;
   cudaError_t e;
   switch (D) {

@@ -146,41 +146,47 @@ fa_bwd_dkv_split_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0 && n_iter > 0) {
-      tma_prefetch_desc(&map_q);
-      tma_prefetch_desc(&map_do);
-      mbar_arrive_expect_tx(bar(B_KVFULL), (C::DO_DK ? 2 : 1) * C::KV_TILE);
+    if (n_iter > 0) {
+      // the whole warp runs the loop (a lone active lane whose siblings wait at
+      // the final barrier issues far slower); one elected lane issues
+      const bool leader = elect_one_sync();
+      if (leader) tma_prefetch_desc(&map_q);
+      if (leader) tma_prefetch_desc(&map_do);
+      if (leader) mbar_arrive_expect_tx(bar(B_KVFULL), (C::DO_DK ? 2 : 1) * C::KV_TILE);
       for (int r = 0; r < C::KREG; ++r) {
-        tma_load_3d(sbase + C::OFF_K + r * C::KV_REGION, &map_k, bar(B_KVFULL), r * 64, k0, bg);
+        if (leader) tma_load_3d(sbase + C::OFF_K + r * C::KV_REGION, &map_k, bar(B_KVFULL), r * 64, k0, bg);
         if (C::DO_DK)
-          tma_load_3d(sbase + C::OFF_V + r * C::KV_REGION, &map_v, bar(B_KVFULL), r * 64, k0, bg);
+          if (leader) tma_load_3d(sbase + C::OFF_V + r * C::KV_REGION, &map_v, bar(B_KVFULL), r * 64, k0, bg);
       }
       for (int it = 0; it < n_iter; ++it) {
         const int st = it % C::STAGES;
         const int h = g * reps + it / n_qt;
         const int i0 = (i_lo + it % n_qt) * C::BMQ;
         if (it >= C::STAGES)
-          mbar_wait(bar(B_QEMPTY + st), ((it / C::STAGES) - 1) & 1, wc.timeout_ns, abort_flag,
+          mbar_wait(bar(B_QEMPTY + st), ((it / C::STAGES) - 1) & 1, wc.timeout_cycles, abort_flag,
                     wc.status);
-        mbar_arrive_expect_tx(bar(B_QFULL + st), 2 * C::Q_TILE);
+        if (leader) mbar_arrive_expect_tx(bar(B_QFULL + st), 2 * C::Q_TILE);
         const int zq = b * s.Hq + h;
         for (int r = 0; r < C::KREG; ++r) {
-          tma_load_3d(sbase + C::OFF_Q + st * C::Q_TILE + r * C::Q_REGION, &map_q,
+          if (leader) tma_load_3d(sbase + C::OFF_Q + st * C::Q_TILE + r * C::Q_REGION, &map_q,
                       bar(B_QFULL + st), r * 64, i0, zq);
-          tma_load_3d(sbase + C::OFF_DO + st * C::Q_TILE + r * C::Q_REGION, &map_do,
+          if (leader) tma_load_3d(sbase + C::OFF_DO + st * C::Q_TILE + r * C::Q_REGION, &map_do,
                       bar(B_QFULL + st), r * 64, i0, zq);
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && n_iter > 0) {
+    if (n_iter > 0) {
+      // the whole warp runs the loop (a lone active lane whose siblings wait at
+      // the final barrier issues far slower); one elected lane issues
+      const bool leader = elect_one_sync();
       constexpr uint32_t ab = C::BF16 ? 1 : 0;
       constexpr uint32_t idesc_st = make_idesc_f16(kBM, C::BMQ, ab, 0, 0);  // S^T, dP^T
       constexpr uint32_t idesc_acc = make_idesc_f16(kBM, C::D, ab, 0, 1);   // dV, dK
-      mbar_wait(bar(B_KVFULL), 0, wc.timeout_ns, abort_flag, wc.status);
+      mbar_wait(bar(B_KVFULL), 0, wc.timeout_cycles, abort_flag, wc.status);
       for (int it = 0; it < n_iter; ++it) {
         const int st = it % C::STAGES;
-        mbar_wait(bar(B_QFULL + st), (it / C::STAGES) & 1, wc.timeout_ns, abort_flag, wc.status);
+        mbar_wait(bar(B_QFULL + st), (it / C::STAGES) & 1, wc.timeout_cycles, abort_flag, wc.status);
         tc_fence_after();
         const uint32_t qa = sbase + C::OFF_Q + st * C::Q_TILE;
         const uint32_t da = sbase + C::OFF_DO + st * C::Q_TILE;
@@ -190,15 +196,15 @@ fa_bwd_dkv_split_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
           const uint32_t off = (kk & 3) * 32;
           const uint64_t bq = make_sdesc(qa + (kk >> 2) * C::Q_REGION + off, 16, 1024, 2);
           const uint64_t ak = make_sdesc(sbase + C::OFF_K + (kk >> 2) * C::KV_REGION + off, 16, 1024, 2);
-          mma_ss(tmem + C::S_COL, ak, bq, idesc_st, kk > 0);
+          if (leader) mma_ss(tmem + C::S_COL, ak, bq, idesc_st, kk > 0);
           if (C::DO_DK) {
             const uint64_t bd = make_sdesc(da + (kk >> 2) * C::Q_REGION + off, 16, 1024, 2);
             const uint64_t av = make_sdesc(sbase + C::OFF_V + (kk >> 2) * C::KV_REGION + off, 16, 1024, 2);
-            mma_ss(tmem + C::DP_COL, av, bd, idesc_st, kk > 0);
+            if (leader) mma_ss(tmem + C::DP_COL, av, bd, idesc_st, kk > 0);
           }
         }
-        mma_commit(bar(B_SFULL));
-        mbar_wait(bar(B_PFULL), it & 1, wc.timeout_ns, abort_flag, wc.status);
+        if (leader) mma_commit(bar(B_SFULL));
+        mbar_wait(bar(B_PFULL), it & 1, wc.timeout_cycles, abort_flag, wc.status);
         tc_fence_after();
         // dV += P^T dO  and  dK += dS^T Q   (A from TMEM, B MN-major, K = query rows)
 #pragma unroll
@@ -206,17 +212,17 @@ fa_bwd_dkv_split_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
           if (C::DO_DV) {
             const uint64_t bd = make_sdesc(da + kk * 16 * 128, C::Q_REGION, 1024, 2);
-            mma_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8, bd, idesc_acc, acc);
+            if (leader) mma_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8, bd, idesc_acc, acc);
           }
           if (C::DO_DK) {
             const uint64_t bq = make_sdesc(qa + kk * 16 * 128, C::Q_REGION, 1024, 2);
-            mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8, bq, idesc_acc, acc);
+            if (leader) mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8, bq, idesc_acc, acc);
           }
         }
-        mma_commit(bar(B_QEMPTY + st));
+        if (leader) mma_commit(bar(B_QEMPTY + st));
       }
-      mma_commit(bar(B_DONE));
-      mbar_wait(bar(B_DONE), 0, wc.timeout_ns, nullptr, wc.status);
+      if (leader) mma_commit(bar(B_DONE));
+      mbar_wait(bar(B_DONE), 0, wc.timeout_cycles, nullptr, wc.status);
     }
   } else if (warp >= 4) {
     const int quarter = warp & 3;
@@ -243,7 +249,7 @@ fa_bwd_dkv_split_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
         dv_s[tid] = dd;
       }
       named_bar_sync(1, 128);
-      mbar_wait(bar(B_SFULL), it & 1, wc.timeout_ns, abort_flag, wc.status);
+      mbar_wait(bar(B_SFULL), it & 1, wc.timeout_cycles, abort_flag, wc.status);
       tc_fence_after();
       const bool need_mask = !block_unmasked(s, i0, i0 + C::BMQ, k0, k0 + kBM);
 #pragma unroll
@@ -279,7 +285,7 @@ fa_bwd_dkv_split_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
       // the last q_empty commit covers every MMA: wait for it through B_DONE's
       // producer-side twin, the final q_empty phase of the last stage
       const int last = n_iter - 1;
-      mbar_wait(bar(B_QEMPTY + last % C::STAGES), (last / C::STAGES) & 1, wc.timeout_ns,
+      mbar_wait(bar(B_QEMPTY + last % C::STAGES), (last / C::STAGES) & 1, wc.timeout_cycles,
                 abort_flag, wc.status);
       tc_fence_after();
     }
@@ -399,39 +405,45 @@ fa_bwd_dq_serial_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0 && n_iter > 0) {
-      tma_prefetch_desc(&map_k);
-      tma_prefetch_desc(&map_v);
-      mbar_arrive_expect_tx(bar(B_QFULL), 2 * C::Q_TILE);
+    if (n_iter > 0) {
+      // the whole warp runs the loop (a lone active lane whose siblings wait at
+      // the final barrier issues far slower); one elected lane issues
+      const bool leader = elect_one_sync();
+      if (leader) tma_prefetch_desc(&map_k);
+      if (leader) tma_prefetch_desc(&map_v);
+      if (leader) mbar_arrive_expect_tx(bar(B_QFULL), 2 * C::Q_TILE);
       for (int r = 0; r < C::KREG; ++r) {
-        tma_load_3d(sbase + C::OFF_Q + r * C::Q_REGION, &map_q, bar(B_QFULL), r * 64, q0, bh);
-        tma_load_3d(sbase + C::OFF_DO + r * C::Q_REGION, &map_do, bar(B_QFULL), r * 64, q0, bh);
+        if (leader) tma_load_3d(sbase + C::OFF_Q + r * C::Q_REGION, &map_q, bar(B_QFULL), r * 64, q0, bh);
+        if (leader) tma_load_3d(sbase + C::OFF_DO + r * C::Q_REGION, &map_do, bar(B_QFULL), r * 64, q0, bh);
       }
       const int zkv = b * s.Hkv + g;
       for (int it = 0; it < n_iter; ++it) {
         const int st = it % C::STAGES;
         if (it >= C::STAGES)
-          mbar_wait(bar(B_KVEMPTY + st), ((it / C::STAGES) - 1) & 1, wc.timeout_ns, abort_flag,
+          mbar_wait(bar(B_KVEMPTY + st), ((it / C::STAGES) - 1) & 1, wc.timeout_cycles, abort_flag,
                     wc.status);
         const int kr = (j_lo + it) * C::BN;
-        mbar_arrive_expect_tx(bar(B_KVFULL + st), 2 * C::KV_TILE);
+        if (leader) mbar_arrive_expect_tx(bar(B_KVFULL + st), 2 * C::KV_TILE);
         for (int r = 0; r < C::KREG; ++r) {
-          tma_load_3d(sbase + C::OFF_K + st * C::KV_TILE + r * C::KV_REGION, &map_k,
+          if (leader) tma_load_3d(sbase + C::OFF_K + st * C::KV_TILE + r * C::KV_REGION, &map_k,
                       bar(B_KVFULL + st), r * 64, kr, zkv);
-          tma_load_3d(sbase + C::OFF_V + st * C::KV_TILE + r * C::KV_REGION, &map_v,
+          if (leader) tma_load_3d(sbase + C::OFF_V + st * C::KV_TILE + r * C::KV_REGION, &map_v,
                       bar(B_KVFULL + st), r * 64, kr, zkv);
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && n_iter > 0) {
+    if (n_iter > 0) {
+      // the whole warp runs the loop (a lone active lane whose siblings wait at
+      // the final barrier issues far slower); one elected lane issues
+      const bool leader = elect_one_sync();
       constexpr uint32_t ab = C::BF16 ? 1 : 0;
       constexpr uint32_t idesc_s = make_idesc_f16(kBM, C::BN, ab, 0, 0);
       constexpr uint32_t idesc_q = make_idesc_f16(kBM, C::D, ab, 0, 1);
-      mbar_wait(bar(B_QFULL), 0, wc.timeout_ns, abort_flag, wc.status);
+      mbar_wait(bar(B_QFULL), 0, wc.timeout_cycles, abort_flag, wc.status);
       for (int it = 0; it < n_iter; ++it) {
         const int st = it % C::STAGES;
-        mbar_wait(bar(B_KVFULL + st), (it / C::STAGES) & 1, wc.timeout_ns, abort_flag, wc.status);
+        mbar_wait(bar(B_KVFULL + st), (it / C::STAGES) & 1, wc.timeout_cycles, abort_flag, wc.status);
         tc_fence_after();
         const uint32_t ka = sbase + C::OFF_K + st * C::KV_TILE;
         const uint32_t va = sbase + C::OFF_V + st * C::KV_TILE;
@@ -441,24 +453,24 @@ fa_bwd_dq_serial_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
           const uint32_t off = (kk & 3) * 32;
           const uint64_t aq = make_sdesc(sbase + C::OFF_Q + (kk >> 2) * C::Q_REGION + off, 16, 1024, 2);
           const uint64_t bk = make_sdesc(ka + (kk >> 2) * C::KV_REGION + off, 16, 1024, 2);
-          mma_ss(tmem + C::S_COL, aq, bk, idesc_s, kk > 0);
+          if (leader) mma_ss(tmem + C::S_COL, aq, bk, idesc_s, kk > 0);
           const uint64_t ad = make_sdesc(sbase + C::OFF_DO + (kk >> 2) * C::Q_REGION + off, 16, 1024, 2);
           const uint64_t bv = make_sdesc(va + (kk >> 2) * C::KV_REGION + off, 16, 1024, 2);
-          mma_ss(tmem + C::DP_COL, ad, bv, idesc_s, kk > 0);
+          if (leader) mma_ss(tmem + C::DP_COL, ad, bv, idesc_s, kk > 0);
         }
-        mma_commit(bar(B_SFULL));
-        mbar_wait(bar(B_PFULL), it & 1, wc.timeout_ns, abort_flag, wc.status);
+        if (leader) mma_commit(bar(B_SFULL));
+        mbar_wait(bar(B_PFULL), it & 1, wc.timeout_cycles, abort_flag, wc.status);
         tc_fence_after();
         // dQ += dS K   (dS from TMEM, K as MN-major B)
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           const uint64_t bk = make_sdesc(ka + kk * 16 * 128, C::KV_REGION, 1024, 2);
-          mma_ts(tmem + C::DQ_COL, tmem + C::S_COL + kk * 8, bk, idesc_q, (it > 0 || kk > 0) ? 1u : 0u);
+          if (leader) mma_ts(tmem + C::DQ_COL, tmem + C::S_COL + kk * 8, bk, idesc_q, (it > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar(B_KVEMPTY + st));
+        if (leader) mma_commit(bar(B_KVEMPTY + st));
       }
-      mma_commit(bar(B_DONE));
-      mbar_wait(bar(B_DONE), 0, wc.timeout_ns, nullptr, wc.status);
+      if (leader) mma_commit(bar(B_DONE));
+      mbar_wait(bar(B_DONE), 0, wc.timeout_cycles, nullptr, wc.status);
     }
   } else if (warp >= 4) {
     const int quarter = warp & 3;
@@ -475,7 +487,7 @@ fa_bwd_dq_serial_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
     }
     for (int it = 0; it < n_iter; ++it) {
       const int kb = (j_lo + it) * C::BN;
-      mbar_wait(bar(B_SFULL), it & 1, wc.timeout_ns, abort_flag, wc.status);
+      mbar_wait(bar(B_SFULL), it & 1, wc.timeout_cycles, abort_flag, wc.status);
       tc_fence_after();
       const bool need_mask = !block_unmasked(s, q0, q0 + kBM, kb, kb + C::BN);
 #pragma unroll
@@ -506,7 +518,7 @@ fa_bwd_dq_serial_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
     }
     if (n_iter > 0) {
       const int last = n_iter - 1;
-      mbar_wait(bar(B_KVEMPTY + last % C::STAGES), (last / C::STAGES) & 1, wc.timeout_ns,
+      mbar_wait(bar(B_KVEMPTY + last % C::STAGES), (last / C::STAGES) & 1, wc.timeout_cycles,
                 abort_flag, wc.status);
       tc_fence_after();
     }

@@ -28,7 +28,7 @@ struct AttnShape {
 
 struct WaitCfg {
   uint32_t* status;    // device status word
-  uint64_t timeout_ns; // bound of every mbarrier wait
+  uint64_t timeout_cycles;  // bound of every mbarrier wait, in SM clock cycles
 };
 
 // Order in which a 1-D grid visits (unit, tile) work items. A unit is a

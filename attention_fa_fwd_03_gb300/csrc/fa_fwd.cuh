@@ -112,35 +112,41 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_iter > 0) {
-      tma_prefetch_desc(&map_q);
-      tma_prefetch_desc(&map_k);
-      tma_prefetch_desc(&map_v);
-      mbar_arrive_expect_tx(bar(B_QFULL), C::NQ * C::Q_TILE);
+    if (n_iter > 0) {
+      // the whole warp runs the loop (a lone active lane whose siblings wait at
+      // the final barrier issues far slower); one elected lane issues
+      const bool leader = elect_one_sync();
+      if (leader) tma_prefetch_desc(&map_q);
+      if (leader) tma_prefetch_desc(&map_k);
+      if (leader) tma_prefetch_desc(&map_v);
+      if (leader) mbar_arrive_expect_tx(bar(B_QFULL), C::NQ * C::Q_TILE);
       for (int t = 0; t < C::NQ; ++t)
         for (int r = 0; r < C::KREG; ++r)
-          tma_load_3d(sbase + C::OFF_Q + t * C::Q_TILE + r * C::Q_REGION, &map_q, bar(B_QFULL),
+          if (leader) tma_load_3d(sbase + C::OFF_Q + t * C::Q_TILE + r * C::Q_REGION, &map_q, bar(B_QFULL),
                       r * 64, q0 + t * kBM, bh);
       const int zkv = b * s.Hkv + g;
       for (int it = 0; it < n_iter; ++it) {
         const int st = it % C::STAGES;
         if (it >= C::STAGES)
-          mbar_wait(bar(B_KVEMPTY + st), ((it / C::STAGES) - 1) & 1, wc.timeout_ns, abort_flag,
+          mbar_wait(bar(B_KVEMPTY + st), ((it / C::STAGES) - 1) & 1, wc.timeout_cycles, abort_flag,
                     wc.status);
         const int krow = (j_lo + it) * C::BN;
-        mbar_arrive_expect_tx(bar(B_KFULL + st), C::KV_TILE);
+        if (leader) mbar_arrive_expect_tx(bar(B_KFULL + st), C::KV_TILE);
         for (int r = 0; r < C::KREG; ++r)
-          tma_load_3d(sbase + C::OFF_K + st * C::KV_TILE + r * C::KV_REGION, &map_k,
+          if (leader) tma_load_3d(sbase + C::OFF_K + st * C::KV_TILE + r * C::KV_REGION, &map_k,
                       bar(B_KFULL + st), r * 64, krow, zkv);
-        mbar_arrive_expect_tx(bar(B_VFULL + st), C::KV_TILE);
+        if (leader) mbar_arrive_expect_tx(bar(B_VFULL + st), C::KV_TILE);
         for (int r = 0; r < C::KREG; ++r)
-          tma_load_3d(sbase + C::OFF_V + st * C::KV_TILE + r * C::KV_REGION, &map_v,
+          if (leader) tma_load_3d(sbase + C::OFF_V + st * C::KV_TILE + r * C::KV_REGION, &map_v,
                       bar(B_VFULL + st), r * 64, krow, zkv);
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
-    if (lane == 0 && n_iter > 0) {
+    if (n_iter > 0) {
+      // the whole warp runs the loop (a lone active lane whose siblings wait at
+      // the final barrier issues far slower); one elected lane issues
+      const bool leader = elect_one_sync();
       constexpr uint32_t idesc_s = make_idesc_f16(kBM, C::BN, C::BF16 ? 1 : 0, 0, 0);
       constexpr uint32_t idesc_o = make_idesc_f16(kBM, C::D, C::BF16 ? 1 : 0, 0, 1);
       auto issue_s = [&](int t, int st) {
@@ -151,7 +157,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           const uint32_t off = (kk & 3) * 32;  // 16 elements = 32 bytes along K
           const uint64_t ad = make_sdesc(qa + (kk >> 2) * C::Q_REGION + off, 16, 1024, 2);
           const uint64_t bd = make_sdesc(ka + (kk >> 2) * C::KV_REGION + off, 16, 1024, 2);
-          mma_ss(tmem + C::S_COL(t), ad, bd, idesc_s, kk > 0);
+          if (leader) mma_ss(tmem + C::S_COL(t), ad, bd, idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int st, bool acc) {
@@ -159,41 +165,41 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           const uint64_t bd = make_sdesc(va + kk * 16 * 128, C::KV_REGION, 1024, 2);
-          mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, bd, idesc_o,
+          if (leader) mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, bd, idesc_o,
                  (acc || kk > 0) ? 1u : 0u);
         }
       };
-      mbar_wait(bar(B_QFULL), 0, wc.timeout_ns, abort_flag, wc.status);
-      mbar_wait(bar(B_KFULL + 0), 0, wc.timeout_ns, abort_flag, wc.status);
+      mbar_wait(bar(B_QFULL), 0, wc.timeout_cycles, abort_flag, wc.status);
+      mbar_wait(bar(B_KFULL + 0), 0, wc.timeout_cycles, abort_flag, wc.status);
       tc_fence_after();
       for (int t = 0; t < C::NQ; ++t) {
-        issue_s(t, 0);
-        mma_commit(bar(B_SFULL + t));
+        if (leader) issue_s(t, 0);
+        if (leader) mma_commit(bar(B_SFULL + t));
       }
       for (int it = 0; it < n_iter; ++it) {
         const int st = it % C::STAGES;
         const int nst = (it + 1) % C::STAGES;
-        mbar_wait(bar(B_VFULL + st), (it / C::STAGES) & 1, wc.timeout_ns, abort_flag, wc.status);
+        mbar_wait(bar(B_VFULL + st), (it / C::STAGES) & 1, wc.timeout_cycles, abort_flag, wc.status);
         for (int t = 0; t < C::NQ; ++t) {
-          mbar_wait(bar(B_PFULL + t), it & 1, wc.timeout_ns, abort_flag, wc.status);
+          mbar_wait(bar(B_PFULL + t), it & 1, wc.timeout_cycles, abort_flag, wc.status);
           tc_fence_after();
-          issue_pv(t, st, it > 0);
-          mma_commit(bar(B_OREADY + t));
+          if (leader) issue_pv(t, st, it > 0);
+          if (leader) mma_commit(bar(B_OREADY + t));
           if (it + 1 < n_iter) {
             if (t == 0) {
-              mbar_wait(bar(B_KFULL + nst), ((it + 1) / C::STAGES) & 1, wc.timeout_ns, abort_flag,
+              mbar_wait(bar(B_KFULL + nst), ((it + 1) / C::STAGES) & 1, wc.timeout_cycles, abort_flag,
                         wc.status);
               tc_fence_after();
             }
-            issue_s(t, nst);
-            mma_commit(bar(B_SFULL + t));
+            if (leader) issue_s(t, nst);
+            if (leader) mma_commit(bar(B_SFULL + t));
           }
         }
-        mma_commit(bar(B_KVEMPTY + st));
+        if (leader) mma_commit(bar(B_KVEMPTY + st));
       }
       // make sure nothing is in flight before TMEM is released
-      mma_commit(bar(B_DRAIN));
-      mbar_wait(bar(B_DRAIN), 0, wc.timeout_ns, nullptr, wc.status);
+      if (leader) mma_commit(bar(B_DRAIN));
+      mbar_wait(bar(B_DRAIN), 0, wc.timeout_cycles, nullptr, wc.status);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------- softmax
@@ -211,7 +217,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     float l = 0.f;
     for (int it = 0; it < n_iter; ++it) {
       const int k0 = (j_lo + it) * C::BN;
-      mbar_wait(bar(B_SFULL + t), it & 1, wc.timeout_ns, abort_flag, wc.status);
+      mbar_wait(bar(B_SFULL + t), it & 1, wc.timeout_cycles, abort_flag, wc.status);
       tc_fence_after();
       uint32_t sr[C::BN];
 #pragma unroll
@@ -254,7 +260,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       l = l * alpha + rs;
       if (it > 0 && __any_sync(0xffffffffu, grow)) {
         // O_t holds the sum of the previous tiles: wait for the last of them.
-        mbar_wait(bar(B_OREADY + t), (it - 1) & 1, wc.timeout_ns, abort_flag, wc.status);
+        mbar_wait(bar(B_OREADY + t), (it - 1) & 1, wc.timeout_cycles, abort_flag, wc.status);
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < C::D; cc += 32) {
@@ -273,7 +279,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 
     // ------------------------------------------------------------ epilogue
     if (n_iter > 0) {
-      mbar_wait(bar(B_OREADY + t), (n_iter - 1) & 1, wc.timeout_ns, abort_flag, wc.status);
+      mbar_wait(bar(B_OREADY + t), (n_iter - 1) & 1, wc.timeout_cycles, abort_flag, wc.status);
       tc_fence_after();
     }
     const bool valid = row < s.Tq;

@@ -112,18 +112,23 @@ cudaError_t launch_dq_with(const BwdLaunch& a, Kern kern) {
   return cudaGetLastError();
 }
 
+// Softmax warpgroups of the pipelined backward kernels: four (32 score columns
+// each) give every SM sub-partition four softmax warps to hide the TMEM and
+// MUFU latencies with.
+constexpr int kSoftmaxWarpgroups = 4;
+
 // Backward for one head dim. D <= 128: the pipelined 128 x 128 kernels
-// (fa_bwd_pipelined.cuh) with KST / QST stages. D = 256: the accumulators
-// alone fill TMEM, so dV and dK run as two passes with 64-row query tiles and
-// dQ with 64-column key tiles, one stage (fa_bwd.cuh).
-template <int D, bool BF16, int KST, int QST>
+// (fa_bwd_pipelined.cuh). D = 256: the accumulators alone fill TMEM, so dV and
+// dK run as two passes with 64-row query tiles and dQ with 64-column key
+// tiles, one stage (fa_bwd.cuh).
+template <int D, bool BF16>
 cudaError_t run_bwd(const BwdLaunch& a, int phases) {
   cudaError_t e = cudaSuccess;
   if (phases & kPhaseDvec) e = run_dvec<D, BF16>(a);
   if (e != cudaSuccess) return e;
   if (phases & kPhaseDkv) {
     if constexpr (D <= 128) {
-      using C = DkvCfg<D, KST, BF16>;
+      using C = DkvCfg<D, BF16, kSoftmaxWarpgroups>;
       e = launch_dkv_with<C>(a, fa_bwd_dkv_kernel<C>);
     } else {
       using CV = DkvSplitCfg<D, 64, 2, BF16, kModeDV>;
@@ -135,7 +140,7 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
   if (e != cudaSuccess) return e;
   if (phases & kPhaseDq) {
     if constexpr (D <= 128) {
-      using C = DqCfg<D, QST, BF16>;
+      using C = DqCfg<D, BF16, kSoftmaxWarpgroups>;
       e = launch_dq_with<C>(a, fa_bwd_dq_kernel<C>);
     } else {
       using C = DqSerialCfg<D, 64, 1, BF16>;
@@ -147,17 +152,16 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
 
 }  // namespace fa
 
-// Define launch_fwd_d<D> / launch_bwd_d<D> for one head dim: forward tile
-// configuration (NQ query tiles per CTA, key tile BN, STAGES), and the stage
-// counts of the pipelined dK/dV and dQ kernels.
-#define FA_DEFINE_HEAD_DIM(D, FNQ, FBN, FST, KST, QST)                                    \
+// Define launch_fwd_d<D> / launch_bwd_d<D> for one head dim, given the forward
+// tile configuration (NQ query tiles per CTA, key tile BN, STAGES of the K/V
+// ring).
+#define FA_DEFINE_HEAD_DIM(D, FNQ, FBN, FST)                                              \
   namespace fa {                                                                          \
   cudaError_t launch_fwd_d##D(const FwdLaunch& a) {                                       \
     return a.bf16 ? run_fwd<FwdCfg<D, FNQ, FBN, FST, true>>(a)                            \
                   : run_fwd<FwdCfg<D, FNQ, FBN, FST, false>>(a);                          \
   }                                                                                       \
   cudaError_t launch_bwd_d##D(const BwdLaunch& a, int phases) {                           \
-    return a.bf16 ? run_bwd<D, true, KST, QST>(a, phases)                                 \
-                  : run_bwd<D, false, KST, QST>(a, phases);                               \
+    return a.bf16 ? run_bwd<D, true>(a, phases) : run_bwd<D, false>(a, phases);           \
   }                                                                                       \
   }

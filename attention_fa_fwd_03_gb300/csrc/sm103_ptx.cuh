@@ -15,8 +15,10 @@ namespace fa {
 
 // ----------------------------------------------------------------- status
 // Device-wide status word. Kernels OR bits into it when a bounded wait gives
-// up; the host reads it through fa_device_status().
-enum : uint32_t { kStatusTimeout = 1u };
+// up (or when the dynamic shared memory they were given is not 1024-byte
+// aligned, which the swizzled layouts need); the host reads it through
+// fa_device_status().
+enum : uint32_t { kStatusTimeout = 1u, kStatusSmemMisaligned = 2u };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -68,26 +70,62 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, giving up after `timeout_ns`.
+// Non-blocking test of phase `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.b32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_wait below, but polling with test_wait: for the single thread that
+// issues MMAs, which must notice a completed phase at once.
+__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity,
+                                               uint64_t timeout_cycles, volatile int* abort,
+                                               uint32_t* status) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (static_cast<uint64_t>(clock64() - t0) > timeout_cycles) {
+      if (abort != nullptr) *abort = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after
+// `timeout_cycles` SM clock cycles (clock64: cheap to read, unlike the global
+// timer, so a waiter never misses a completion while reading the clock).
 // On timeout the device status gets kStatusTimeout, `*abort` (a flag in shared
 // memory, shared by the CTA) is raised, and the call returns false. Once the
 // flag is up every later wait returns false at once, so all roles run to the
 // common exit without blocking. `abort` may be null (a drain wait at exit that
 // must not be cut short by an earlier abort).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_cycles,
                                           volatile int* abort, uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (true) {
+#pragma unroll 1
+  for (int i = 0; i < 32; ++i)
     if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 63u) == 0) {
-      if (abort != nullptr && *abort) return false;
-      if (globaltimer_ns() - t0 > timeout_ns) {
-        if (abort != nullptr) *abort = 1;
-        atomicOr(status, kStatusTimeout);
-        return false;
-      }
+  const long long t0 = clock64();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (static_cast<uint64_t>(clock64() - t0) > timeout_cycles) {
+      if (abort != nullptr) *abort = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
     }
   }
 }
