@@ -176,35 +176,39 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == 2) {
+    // ----------------------------------------------------------- producers
+    // warp 0: K, V once, then the Q ring; warp 2: the dO ring. A tile pair
+    // takes ~1.4 us to land under full load, so each ring is refilled the
+    // moment its own slot frees, independently of the other.
     if (n_iter > 0) {
       // the whole warp runs the loop (a lone active lane whose siblings wait at
       // the final barrier issues far slower); one elected lane issues
       const bool leader = elect_one_sync();
-      if (leader) tma_prefetch_desc(&map_q);
-      if (leader) tma_prefetch_desc(&map_do);
-      if (leader) mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE);
-      for (int r = 0; r < C::KREG; ++r) {
-        if (leader) tma_load_3d(sbase + C::OFF_K + r * C::REGION, &map_k, bar(C::B_KVFULL), r * 64, k0, bg);
-        if (leader) tma_load_3d(sbase + C::OFF_V + r * C::REGION, &map_v, bar(C::B_KVFULL), r * 64, k0, bg);
+      const bool q_ring = warp == 0;
+      if (q_ring) {
+        if (leader) tma_prefetch_desc(&map_q);
+        if (leader) mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE);
+        for (int r = 0; r < C::KREG; ++r) {
+          if (leader) tma_load_3d(sbase + C::OFF_K + r * C::REGION, &map_k, bar(C::B_KVFULL), r * 64, k0, bg);
+          if (leader) tma_load_3d(sbase + C::OFF_V + r * C::REGION, &map_v, bar(C::B_KVFULL), r * 64, k0, bg);
+        }
+      } else if (leader) {
+        tma_prefetch_desc(&map_do);
       }
+      const int nst = q_ring ? C::QST : C::DST;
+      const int full = q_ring ? C::B_QFULL : C::B_DOFULL, empty = q_ring ? C::B_QEMPTY : C::B_DOEMPTY;
+      const uint32_t ring = sbase + (q_ring ? C::OFF_Q : C::OFF_DO);
+      const CUtensorMap* map = q_ring ? &map_q : &map_do;
       for (int it = 0; it < n_iter; ++it) {
         const int zq = b * s.Hq + g * reps + it / n_qt;
         const int i0 = (i_lo + it % n_qt) * C::BMQ;
-        const int qs = it % C::QST, ds = it % C::DST;
-        if (it >= C::QST)
-          mbar_wait(bar(C::B_QEMPTY + qs), ((it / C::QST) - 1) & 1, tmo, abort_flag, wc.status);
-        if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::TILE);
+        const int st = it % nst;
+        if (it >= nst)
+          mbar_wait_poll(bar(empty + st), ((it / nst) - 1) & 1, tmo, abort_flag, wc.status);
+        if (leader) mbar_arrive_expect_tx(bar(full + st), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(sbase + C::OFF_Q + qs * C::TILE + r * C::REGION, &map_q,
-                      bar(C::B_QFULL + qs), r * 64, i0, zq);
-        if (it >= C::DST)
-          mbar_wait(bar(C::B_DOEMPTY + ds), ((it / C::DST) - 1) & 1, tmo, abort_flag, wc.status);
-        if (leader) mbar_arrive_expect_tx(bar(C::B_DOFULL + ds), C::TILE);
-        for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(sbase + C::OFF_DO + ds * C::TILE + r * C::REGION, &map_do,
-                      bar(C::B_DOFULL + ds), r * 64, i0, zq);
+          if (leader) tma_load_3d(ring + st * C::TILE + r * C::REGION, map, bar(full + st), r * 64, i0, zq);
       }
     }
   } else if (warp == 1) {
@@ -227,12 +231,12 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           if (leader) mma_ss(tmem + col, ad + (off >> 4), bd + (off >> 4), idesc_st, kk > 0);
         }
       };
-      mbar_wait(bar(C::B_KVFULL), 0, tmo, abort_flag, wc.status);
-      mbar_wait(bar(C::B_QFULL + 0), 0, tmo, abort_flag, wc.status);
+      mbar_wait_poll(bar(C::B_KVFULL), 0, tmo, abort_flag, wc.status);
+      mbar_wait_poll(bar(C::B_QFULL + 0), 0, tmo, abort_flag, wc.status);
       tc_fence_after();
       if (leader) issue_score(sbase + C::OFF_K, sbase + C::OFF_Q, C::S_COL);
       if (leader) mma_commit(bar(C::B_SFULL));
-      mbar_wait(bar(C::B_DOFULL + 0), 0, tmo, abort_flag, wc.status);
+      mbar_wait_poll(bar(C::B_DOFULL + 0), 0, tmo, abort_flag, wc.status);
       tc_fence_after();
       if (leader) issue_score(sbase + C::OFF_V, sbase + C::OFF_DO, C::DP_COL);
       if (leader) mma_commit(bar(C::B_DPFULL));
@@ -242,13 +246,13 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (more) {
           // next S^T as soon as the softmax has read this tile's S^T
           const int nq = (it + 1) % C::QST;
-          mbar_wait(bar(C::B_QFULL + nq), ((it + 1) / C::QST) & 1, tmo, abort_flag, wc.status);
-          mbar_wait(bar(C::B_SFREE), it & 1, tmo, abort_flag, wc.status);
+          mbar_wait_poll(bar(C::B_QFULL + nq), ((it + 1) / C::QST) & 1, tmo, abort_flag, wc.status);
+          mbar_wait_poll(bar(C::B_SFREE), it & 1, tmo, abort_flag, wc.status);
           tc_fence_after();
           if (leader) issue_score(sbase + C::OFF_K, sbase + C::OFF_Q + nq * C::TILE, C::S_COL);
           if (leader) mma_commit(bar(C::B_SFULL));
         }
-        mbar_wait(bar(C::B_PFULL), it & 1, tmo, abort_flag, wc.status);
+        mbar_wait_poll(bar(C::B_PFULL), it & 1, tmo, abort_flag, wc.status);
         tc_fence_after();
         // dK += dS^T Q, then dV += P^T dO  (A from TMEM, B MN-major, K = query rows);
         // each ring slot is released by the last MMA that reads it
@@ -268,14 +272,14 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           // dP^T(it+1) overwrites the P^T / dS^T columns the MMAs above read
           // (tcgen05 MMAs of one thread execute in order)
           const int nd = (it + 1) % C::DST;
-          mbar_wait(bar(C::B_DOFULL + nd), ((it + 1) / C::DST) & 1, tmo, abort_flag, wc.status);
+          mbar_wait_poll(bar(C::B_DOFULL + nd), ((it + 1) / C::DST) & 1, tmo, abort_flag, wc.status);
           tc_fence_after();
           if (leader) issue_score(sbase + C::OFF_V, sbase + C::OFF_DO + nd * C::TILE, C::DP_COL);
           if (leader) mma_commit(bar(C::B_DPFULL));
         }
       }
       if (leader) mma_commit(bar(C::B_DONE));
-      mbar_wait(bar(C::B_DONE), 0, tmo, nullptr, wc.status);
+      mbar_wait_poll(bar(C::B_DONE), 0, tmo, nullptr, wc.status);
     }
   } else if (warp == 3) {
     // ------------------------------------------- LSE / D-vector staging
@@ -470,34 +474,37 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
+    // producers: warp 0 loads Q, dO once, then the K ring; warp 2 the V ring,
+    // each refilled the moment its own slot frees
     if (n_iter > 0) {
       // the whole warp runs the loop (a lone active lane whose siblings wait at
       // the final barrier issues far slower); one elected lane issues
       const bool leader = elect_one_sync();
-      if (leader) tma_prefetch_desc(&map_k);
-      if (leader) tma_prefetch_desc(&map_v);
-      if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE);
-      for (int r = 0; r < C::KREG; ++r) {
-        if (leader) tma_load_3d(sbase + C::OFF_Q + r * C::REGION, &map_q, bar(C::B_QFULL), r * 64, q0, bh);
-        if (leader) tma_load_3d(sbase + C::OFF_DO + r * C::REGION, &map_do, bar(C::B_QFULL), r * 64, q0, bh);
+      const bool k_ring = warp == 0;
+      if (k_ring) {
+        if (leader) tma_prefetch_desc(&map_k);
+        if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE);
+        for (int r = 0; r < C::KREG; ++r) {
+          if (leader) tma_load_3d(sbase + C::OFF_Q + r * C::REGION, &map_q, bar(C::B_QFULL), r * 64, q0, bh);
+          if (leader) tma_load_3d(sbase + C::OFF_DO + r * C::REGION, &map_do, bar(C::B_QFULL), r * 64, q0, bh);
+        }
+      } else if (leader) {
+        tma_prefetch_desc(&map_v);
       }
       const int zkv = b * s.Hkv + g;
+      const int nst = k_ring ? C::KST : C::VST;
+      const int full = k_ring ? C::B_KFULL : C::B_VFULL, empty = k_ring ? C::B_KEMPTY : C::B_VEMPTY;
+      const uint32_t ring = sbase + (k_ring ? C::OFF_K : C::OFF_V);
+      const CUtensorMap* map = k_ring ? &map_k : &map_v;
       for (int it = 0; it < n_iter; ++it) {
         const int kr = (j_lo + it) * C::BN;
-        const int ks = it % C::KST, vs = it % C::VST;
-        if (it >= C::KST)
-          mbar_wait(bar(C::B_KEMPTY + ks), ((it / C::KST) - 1) & 1, tmo, abort_flag, wc.status);
-        if (leader) mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::TILE);
+        const int st = it % nst;
+        if (it >= nst)
+          mbar_wait_poll(bar(empty + st), ((it / nst) - 1) & 1, tmo, abort_flag, wc.status);
+        if (leader) mbar_arrive_expect_tx(bar(full + st), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(sbase + C::OFF_K + ks * C::TILE + r * C::REGION, &map_k,
-                      bar(C::B_KFULL + ks), r * 64, kr, zkv);
-        if (it >= C::VST)
-          mbar_wait(bar(C::B_VEMPTY + vs), ((it / C::VST) - 1) & 1, tmo, abort_flag, wc.status);
-        if (leader) mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::TILE);
-        for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(sbase + C::OFF_V + vs * C::TILE + r * C::REGION, &map_v,
-                      bar(C::B_VFULL + vs), r * 64, kr, zkv);
+          if (leader) tma_load_3d(ring + st * C::TILE + r * C::REGION, map, bar(full + st), r * 64, kr, zkv);
       }
     }
   } else if (warp == 1) {
@@ -516,12 +523,12 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
           if (leader) mma_ss(tmem + col, ad + (off >> 4), bd + (off >> 4), idesc_s, kk > 0);
         }
       };
-      mbar_wait(bar(C::B_QFULL), 0, tmo, abort_flag, wc.status);
-      mbar_wait(bar(C::B_KFULL + 0), 0, tmo, abort_flag, wc.status);
+      mbar_wait_poll(bar(C::B_QFULL), 0, tmo, abort_flag, wc.status);
+      mbar_wait_poll(bar(C::B_KFULL + 0), 0, tmo, abort_flag, wc.status);
       tc_fence_after();
       if (leader) issue_score(sbase + C::OFF_Q, sbase + C::OFF_K, C::S_COL);
       if (leader) mma_commit(bar(C::B_SFULL));
-      mbar_wait(bar(C::B_VFULL + 0), 0, tmo, abort_flag, wc.status);
+      mbar_wait_poll(bar(C::B_VFULL + 0), 0, tmo, abort_flag, wc.status);
       tc_fence_after();
       if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V, C::DP_COL);
       if (leader) mma_commit(bar(C::B_DPFULL));
@@ -531,13 +538,13 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         const bool more = it + 1 < n_iter;
         if (more) {
           const int nk = (it + 1) % C::KST;
-          mbar_wait(bar(C::B_KFULL + nk), ((it + 1) / C::KST) & 1, tmo, abort_flag, wc.status);
-          mbar_wait(bar(C::B_SFREE), it & 1, tmo, abort_flag, wc.status);
+          mbar_wait_poll(bar(C::B_KFULL + nk), ((it + 1) / C::KST) & 1, tmo, abort_flag, wc.status);
+          mbar_wait_poll(bar(C::B_SFREE), it & 1, tmo, abort_flag, wc.status);
           tc_fence_after();
           if (leader) issue_score(sbase + C::OFF_Q, sbase + C::OFF_K + nk * C::TILE, C::S_COL);
           if (leader) mma_commit(bar(C::B_SFULL));
         }
-        mbar_wait(bar(C::B_PFULL), it & 1, tmo, abort_flag, wc.status);
+        mbar_wait_poll(bar(C::B_PFULL), it & 1, tmo, abort_flag, wc.status);
         tc_fence_after();
         // dQ += dS K   (dS from TMEM, K as MN-major B, K = key rows)
         const uint64_t kdesc = make_sdesc(sbase + C::OFF_K + ks * C::TILE, C::REGION, 1024, 2);
@@ -549,7 +556,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         if (more) {
           // dP(it+1) overwrites the dS columns the MMAs above read (in order)
           const int nv = (it + 1) % C::VST;
-          mbar_wait(bar(C::B_VFULL + nv), ((it + 1) / C::VST) & 1, tmo, abort_flag, wc.status);
+          mbar_wait_poll(bar(C::B_VFULL + nv), ((it + 1) / C::VST) & 1, tmo, abort_flag, wc.status);
           tc_fence_after();
           if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V + nv * C::TILE, C::DP_COL);
           if (leader) mma_commit(bar(C::B_DPFULL));
@@ -557,7 +564,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         }
       }
       if (leader) mma_commit(bar(C::B_DONE));
-      mbar_wait(bar(C::B_DONE), 0, tmo, nullptr, wc.status);
+      mbar_wait_poll(bar(C::B_DONE), 0, tmo, nullptr, wc.status);
     }
   } else if (warp >= 4) {
     const int wg = (warp - 4) >> 2;  // key columns [32 wg, 32 wg + 32)
