@@ -22,13 +22,27 @@
 // * The operand the next tile needs first (Q in dK/dV, K in dQ) is
 //   prefetched three tiles deep, the other two deep, each slot released by
 //   the MMA that last reads it.
+// * Persistent CTAs: the grid has one CTA per work item (row block of the
+//   TileOrder), but a running CTA does not exit after its item: it takes
+//   over the next not-yet-started CTA's item through cluster launch control
+//   (ItemQueue), so one CTA per SM serves a dynamically balanced stream of
+//   items in launch order. Tiles stream through the rings without a break
+//   between items, so the next item's first score block is computed while
+//   the softmax warps still finish (and store) the previous one; the operand
+//   loaded once per item (K, V in dK/dV; Q, dO in dQ) is reloaded as soon as
+//   the item's last MMA that reads it completes. dQ alternates between two
+//   TMEM accumulators so its store overlaps the next item; the dK/dV
+//   accumulators fill TMEM, and the softmax warps store them before they
+//   release the next item's first P/dS block.
 // NWG softmax warpgroups split the 128 columns of every tile (128 / NWG each).
 //
-// TMEM layout of the 16-bit operands: the score columns are handled in chunks
-// of 32; chunk m (loaded from dP columns DP_COL + 32m ..) writes its outputs
-// back to DP_COL + 32m: P^T to [+0, +16) and dS^T to [+16, +32) in dK/dV, dS
-// to [+0, +16) in dQ. So the 16-row K-block kk of the next MMA reads column
-// DP_COL + 32 (kk / 2) + 8 (kk % 2).
+// TMEM layout of the 16-bit operands (written over the dP block they derive
+// from). dK/dV: the 16 query columns of K-block kk of the accumulating MMAs
+// come from dP^T columns DP_COL + 16 kk ..; their P^T (8 columns of packed
+// pairs) goes to DP_COL + 16 kk and their dS^T to DP_COL + 16 kk + 8, so each
+// 16-column half is read, then overwritten. dQ: the score columns are handled
+// in chunks of 32; chunk m (from dP columns DP_COL + 32m ..) writes its dS to
+// [+0, +16), so K-block kk reads DP_COL + 32 (kk / 2) + 8 (kk % 2).
 #pragma once
 
 #include <type_traits>
@@ -83,7 +97,38 @@ __device__ __forceinline__ void exp2_scores32(uint32_t (&sv)[32], uint64_t c2, c
   }
 }
 
+// After an abort, wait (bounded, whatever the abort flag says) until the last
+// `nst` loads issued into a ring of `nst` slots have landed, so that no copy is
+// still in flight into this CTA's shared memory when it exits.
+__device__ __forceinline__ void drain_ring(uint32_t full_bar0, int nst, int issued,
+                                           uint64_t tmo, uint32_t* status) {
+  for (int i = issued > nst ? issued - nst : 0; i < issued; ++i)
+    mbar_wait(full_bar0 + 8u * static_cast<uint32_t>(i % nst), (i / nst) & 1, tmo, nullptr, status);
+}
+
 // ---------------------------------------------------------------- dK / dV
+// One dK/dV work item: a (batch, KV group) and a block of 128 KV rows; its
+// tiles are the query tiles (of every head of the group) that see the block.
+struct DkvItem {
+  int bg, b, g, k0, i_lo, n_qt, n_iter;
+};
+
+__device__ __forceinline__ DkvItem dkv_item(int linear, const TileOrder& o, const AttnShape& s,
+                                            int bmq) {
+  DkvItem t;
+  int kvt;
+  decode_tile(linear, o, &t.bg, &kvt);
+  t.b = t.bg / s.Hkv;
+  t.g = t.bg - t.b * s.Hkv;
+  t.k0 = kvt * kBM;
+  int qf, ql;
+  query_range(s, t.k0, min(s.Tkv, t.k0 + kBM), &qf, &ql);
+  t.i_lo = qf / bmq;
+  t.n_qt = max(0, (ql + bmq - 1) / bmq - t.i_lo);
+  t.n_iter = t.n_qt * (s.Hq / s.Hkv);
+  return t;
+}
+
 template <int D_, bool BF16_, int NWG_>
 struct DkvCfg {
   static constexpr int D = D_;
@@ -103,27 +148,34 @@ struct DkvCfg {
   static constexpr int OFF_DO = OFF_Q + QST * TILE;
   static constexpr int OFF_STATS = OFF_DO + DST * TILE;  // [2][-lse2 | -dvec][128] fp32
   static constexpr int OFF_BAR = OFF_STATS + 2 * 2 * BMQ * 4;
-  // barriers: kv_full, q_full[QST], q_empty[QST], do_full[DST], do_empty[DST],
-  // stats_full[2], stats_empty[2], s_full, s_free, dp_full, p_full, done
-  static constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = B_QFULL + QST,
-                       B_DOFULL = B_QEMPTY + QST, B_DOEMPTY = B_DOFULL + DST,
-                       B_STFULL = B_DOEMPTY + DST, B_STEMPTY = B_STFULL + 2,
-                       B_SFULL = B_STEMPTY + 2, B_SFREE = B_SFULL + 1, B_DPFULL = B_SFULL + 2,
-                       B_PFULL = B_SFULL + 3, B_DONE = B_SFULL + 4, NBAR = B_DONE + 1;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  // barriers: k_full, k_empty, v_full, v_empty, q_full[QST], q_empty[QST],
+  // do_full[DST], do_empty[DST], stats_full[2], stats_empty[2], s_full, s_free,
+  // dp_full, p_full, done, drain
+  static constexpr int B_KFULL = 0, B_KEMPTY = 1, B_VFULL = 2, B_VEMPTY = 3, B_QFULL = 4,
+                       B_QEMPTY = B_QFULL + QST, B_DOFULL = B_QEMPTY + QST,
+                       B_DOEMPTY = B_DOFULL + DST, B_STFULL = B_DOEMPTY + DST,
+                       B_STEMPTY = B_STFULL + 2, B_SFULL = B_STEMPTY + 2, B_SFREE = B_SFULL + 1,
+                       B_DPFULL = B_SFULL + 2, B_PFULL = B_SFULL + 3, B_DONE = B_SFULL + 4,
+                       B_DRAIN = B_SFULL + 5, B_CLCFULL = B_DRAIN + 1,
+                       B_CLCEMPTY = B_CLCFULL + kClcSlots, NBAR = B_CLCEMPTY + kClcSlots;
+  static constexpr int OFF_CLC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // item responses
+  static constexpr int OFF_MISC = OFF_CLC + 16 * kClcSlots;
   static constexpr int SMEM_BYTES = OFF_MISC + 16;  // base must be 1024-aligned (checked)
   static constexpr int THREADS = 128 + 128 * NWG;
   static constexpr int S_COL = 0;     // S^T block, 128 fp32 columns
   static constexpr int DP_COL = 128;  // dP^T block, 128 fp32 columns
   static constexpr int DV_COL = 256;
   static constexpr int DK_COL = 256 + D;
-  static constexpr uint32_t pt_col(int kk) { return chunk_operand_col(DP_COL, kk); }
-  static constexpr uint32_t dst_col(int kk) { return chunk_operand_col(DP_COL, kk) + 16; }
+  static constexpr uint32_t pt_col(int kk) { return DP_COL + 16 * kk; }
+  static constexpr uint32_t dst_col(int kk) { return DP_COL + 16 * kk + 8; }
   static_assert(NWG == 4, "one 32-column chunk per softmax warpgroup");
   static_assert(D <= 128, "dV and dK accumulators share 256 TMEM columns");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
+// Persistent (see ItemQueue): every role walks the same item stream and counts
+// tiles across items, so the ring slots and barrier phases run on from one
+// item to the next.
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
 fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -144,17 +196,8 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   float* stats = reinterpret_cast<float*>(smem + C::OFF_STATS);
   const uint64_t tmo = wc.timeout_cycles;
-
-  int bg, kvt;  // (b * Hkv + g, block of 128 KV rows)
-  decode_tile(blockIdx.x, order, &bg, &kvt);
-  const int b = bg / s.Hkv, g = bg % s.Hkv;
   const int reps = s.Hq / s.Hkv;
-  const int k0 = kvt * kBM;
-  int qf, ql;
-  query_range(s, k0, min(s.Tkv, k0 + kBM), &qf, &ql);
-  const int i_lo = qf / C::BMQ;
-  const int n_qt = max(0, (ql + C::BMQ - 1) / C::BMQ - i_lo);
-  const int n_iter = n_qt * reps;
+  const ItemQueue iq{sbase + C::OFF_CLC, bar(C::B_CLCFULL), bar(C::B_CLCEMPTY)};
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -163,6 +206,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (i == C::B_STFULL || i == C::B_STFULL + 1) cnt = 32;  // the staging warp's lanes
       if (i == C::B_STEMPTY || i == C::B_STEMPTY + 1 || i == C::B_SFREE || i == C::B_PFULL)
         cnt = 4 * C::NWG;  // one arrival per softmax warp
+      if (i >= C::B_CLCEMPTY && i < C::B_CLCEMPTY + kClcSlots) cnt = C::THREADS / 32;
       mbar_init(bar(i), cnt);
     }
     fence_mbar_init();
@@ -178,209 +222,308 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
   if (warp == 0 || warp == 2) {
     // ----------------------------------------------------------- producers
-    // warp 0: K, V once, then the Q ring; warp 2: the dO ring. A tile pair
-    // takes ~1.4 us to land under full load, so each ring is refilled the
-    // moment its own slot frees, independently of the other.
-    if (n_iter > 0) {
-      // the whole warp runs the loop (a lone active lane whose siblings wait at
-      // the final barrier issues far slower); one elected lane issues
-      const bool leader = elect_one_sync();
-      const bool q_ring = warp == 0;
+    // warp 0: K of each item, then the item's Q ring tiles (and the item
+    // requests); warp 2: V, then the dO ring. A tile pair takes ~1.4 us to
+    // land under full load, so each ring is refilled the moment its own slot
+    // frees. The whole warp runs the loop (a lone active lane whose siblings
+    // wait at the final barrier issues far slower); one elected lane issues.
+    const bool leader = elect_one_sync();
+    const bool q_ring = warp == 0;
+    if (leader) tma_prefetch_desc(q_ring ? &map_q : &map_do);
+    const int nst = q_ring ? C::QST : C::DST;
+    const int full = q_ring ? C::B_QFULL : C::B_DOFULL, empty = q_ring ? C::B_QEMPTY : C::B_DOEMPTY;
+    const int once_full = q_ring ? C::B_KFULL : C::B_VFULL, once_empty = q_ring ? C::B_KEMPTY : C::B_VEMPTY;
+    const uint32_t ring = sbase + (q_ring ? C::OFF_Q : C::OFF_DO);
+    const uint32_t once = sbase + (q_ring ? C::OFF_K : C::OFF_V);
+    const CUtensorMap* map = q_ring ? &map_q : &map_do;
+    const CUtensorMap* once_map = q_ring ? &map_k : &map_v;
+    int gt = 0, ln = 0, asked = 0;  // ring tiles issued, items with work, item requests
+    bool ok = true;
+    for (int k = 0, item = blockIdx.x; ok; ++k) {
       if (q_ring) {
-        if (leader) tma_prefetch_desc(&map_q);
-        if (leader) mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE);
-        for (int r = 0; r < C::KREG; ++r) {
-          if (leader) tma_load_3d(sbase + C::OFF_K + r * C::REGION, &map_k, bar(C::B_KVFULL), r * 64, k0, bg);
-          if (leader) tma_load_3d(sbase + C::OFF_V + r * C::REGION, &map_v, bar(C::B_KVFULL), r * 64, k0, bg);
-        }
-      } else if (leader) {
-        tma_prefetch_desc(&map_do);
+        ok = clc_request(iq, k, leader, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        ++asked;
       }
-      const int nst = q_ring ? C::QST : C::DST;
-      const int full = q_ring ? C::B_QFULL : C::B_DOFULL, empty = q_ring ? C::B_QEMPTY : C::B_DOEMPTY;
-      const uint32_t ring = sbase + (q_ring ? C::OFF_Q : C::OFF_DO);
-      const CUtensorMap* map = q_ring ? &map_q : &map_do;
-      for (int it = 0; it < n_iter; ++it) {
-        const int zq = b * s.Hq + g * reps + it / n_qt;
-        const int i0 = (i_lo + it % n_qt) * C::BMQ;
-        const int st = it % nst;
-        if (it >= nst)
-          mbar_wait_poll(bar(empty + st), ((it / nst) - 1) & 1, tmo, abort_flag, wc.status);
-        if (leader) mbar_arrive_expect_tx(bar(full + st), C::TILE);
+      const DkvItem t = dkv_item(item, order, s, C::BMQ);
+      if (t.n_iter > 0) {
+        // K (or V) of this KV block, once its previous contents were last read
+        if (ln > 0) ok = mbar_wait_poll(bar(once_empty), (ln - 1) & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        if (leader) mbar_arrive_expect_tx(bar(once_full), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(ring + st * C::TILE + r * C::REGION, map, bar(full + st), r * 64, i0, zq);
+          if (leader) tma_load_3d(once + r * C::REGION, once_map, bar(once_full), r * 64, t.k0, t.bg);
+        ++ln;
+        for (int it = 0; it < t.n_iter; ++it, ++gt) {
+          const int zq = t.b * s.Hq + t.g * reps + it / t.n_qt;
+          const int i0 = (t.i_lo + it % t.n_qt) * C::BMQ;
+          const int st = gt % nst;
+          if (gt >= nst) ok = mbar_wait_poll(bar(empty + st), ((gt / nst) - 1) & 1, tmo, abort_flag, wc.status);
+          if (!ok) break;
+          if (leader) mbar_arrive_expect_tx(bar(full + st), C::TILE);
+          for (int r = 0; r < C::KREG; ++r)
+            if (leader) tma_load_3d(ring + st * C::TILE + r * C::REGION, map, bar(full + st), r * 64, i0, zq);
+        }
+        if (!ok) break;
       }
+      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
+    }
+    if (*abort_flag) {
+      drain_ring(bar(once_full), 1, ln, tmo, wc.status);
+      drain_ring(bar(full), nst, gt, tmo, wc.status);
+      if (q_ring) drain_ring(iq.full, kClcSlots, asked, tmo, wc.status);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
-    if (n_iter > 0) {
-      // the whole warp runs the loop (a lone active lane whose siblings wait at
-      // the final barrier issues far slower); one elected lane issues
-      const bool leader = elect_one_sync();
-      constexpr uint32_t ab = C::BF16 ? 1 : 0;
-      constexpr uint32_t idesc_st = make_idesc_f16(kBM, C::BMQ, ab, 0, 0);  // S^T, dP^T
-      constexpr uint32_t idesc_acc = make_idesc_f16(kBM, C::D, ab, 0, 1);   // dV, dK
-      // S^T = K Q^T (into S_COL) or dP^T = V dO^T (into DP_COL): K-major, K = head dim.
-      // Descriptors are built once per operand base; the k-step offsets are
-      // added to the start-address field (shared addresses < 256 KB never carry).
-      auto issue_score = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
-        const uint64_t ad = make_sdesc(a_base, 16, 1024, 2), bd = make_sdesc(b_base, 16, 1024, 2);
+    // the whole warp runs the loop; one elected lane issues
+    const bool leader = elect_one_sync();
+    constexpr uint32_t ab = C::BF16 ? 1 : 0;
+    constexpr uint32_t idesc_st = make_idesc_f16(kBM, C::BMQ, ab, 0, 0);  // S^T, dP^T
+    constexpr uint32_t idesc_acc = make_idesc_f16(kBM, C::D, ab, 0, 1);   // dV, dK
+    // S^T = K Q^T (into S_COL) or dP^T = V dO^T (into DP_COL): K-major, K = head dim.
+    // Descriptors are built once per operand base; the k-step offsets are
+    // added to the start-address field (shared addresses < 256 KB never carry).
+    auto issue_score = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
+      const uint64_t ad = make_sdesc(a_base, 16, 1024, 2), bd = make_sdesc(b_base, 16, 1024, 2);
 #pragma unroll
-        for (int kk = 0; kk < C::D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::REGION + (kk & 3) * 32;
-          if (leader) mma_ss(tmem + col, ad + (off >> 4), bd + (off >> 4), idesc_st, kk > 0);
-        }
-      };
-      mbar_wait_poll(bar(C::B_KVFULL), 0, tmo, abort_flag, wc.status);
-      mbar_wait_poll(bar(C::B_QFULL + 0), 0, tmo, abort_flag, wc.status);
-      tc_fence_after();
-      if (leader) issue_score(sbase + C::OFF_K, sbase + C::OFF_Q, C::S_COL);
-      if (leader) mma_commit(bar(C::B_SFULL));
-      mbar_wait_poll(bar(C::B_DOFULL + 0), 0, tmo, abort_flag, wc.status);
-      tc_fence_after();
-      if (leader) issue_score(sbase + C::OFF_V, sbase + C::OFF_DO, C::DP_COL);
-      if (leader) mma_commit(bar(C::B_DPFULL));
-      for (int it = 0; it < n_iter; ++it) {
-        const int qs = it % C::QST, ds = it % C::DST;
-        const bool more = it + 1 < n_iter;
-        if (more) {
-          // next S^T as soon as the softmax has read this tile's S^T
-          const int nq = (it + 1) % C::QST;
-          mbar_wait_poll(bar(C::B_QFULL + nq), ((it + 1) / C::QST) & 1, tmo, abort_flag, wc.status);
-          mbar_wait_poll(bar(C::B_SFREE), it & 1, tmo, abort_flag, wc.status);
-          tc_fence_after();
-          if (leader) issue_score(sbase + C::OFF_K, sbase + C::OFF_Q + nq * C::TILE, C::S_COL);
-          if (leader) mma_commit(bar(C::B_SFULL));
-        }
-        mbar_wait_poll(bar(C::B_PFULL), it & 1, tmo, abort_flag, wc.status);
-        tc_fence_after();
-        // dK += dS^T Q, then dV += P^T dO  (A from TMEM, B MN-major, K = query rows);
-        // each ring slot is released by the last MMA that reads it
-        const uint64_t qdesc = make_sdesc(sbase + C::OFF_Q + qs * C::TILE, C::REGION, 1024, 2);
-        const uint64_t ddesc = make_sdesc(sbase + C::OFF_DO + ds * C::TILE, C::REGION, 1024, 2);
-#pragma unroll
-        for (int kk = 0; kk < C::BMQ / 16; ++kk)
-          if (leader) mma_ts(tmem + C::DK_COL, tmem + C::dst_col(kk), qdesc + ((kk * 16 * 128) >> 4),
-                 idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
-        if (leader) mma_commit(bar(C::B_QEMPTY + qs));
-#pragma unroll
-        for (int kk = 0; kk < C::BMQ / 16; ++kk)
-          if (leader) mma_ts(tmem + C::DV_COL, tmem + C::pt_col(kk), ddesc + ((kk * 16 * 128) >> 4),
-                 idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
-        if (leader) mma_commit(bar(C::B_DOEMPTY + ds));
-        if (more) {
-          // dP^T(it+1) overwrites the P^T / dS^T columns the MMAs above read
-          // (tcgen05 MMAs of one thread execute in order)
-          const int nd = (it + 1) % C::DST;
-          mbar_wait_poll(bar(C::B_DOFULL + nd), ((it + 1) / C::DST) & 1, tmo, abort_flag, wc.status);
-          tc_fence_after();
-          if (leader) issue_score(sbase + C::OFF_V, sbase + C::OFF_DO + nd * C::TILE, C::DP_COL);
-          if (leader) mma_commit(bar(C::B_DPFULL));
-        }
+      for (int kk = 0; kk < C::D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::REGION + (kk & 3) * 32;
+        if (leader) mma_ss(tmem + col, ad + (off >> 4), bd + (off >> 4), idesc_st, kk > 0);
       }
-      if (leader) mma_commit(bar(C::B_DONE));
-      mbar_wait_poll(bar(C::B_DONE), 0, tmo, nullptr, wc.status);
+    };
+    auto wait = [&](int b, int parity) {
+      return mbar_wait_poll(bar(b), parity & 1, tmo, abort_flag, wc.status);
+    };
+    int gt = 0, ln = 0;  // tiles before this item, items with work
+    bool ok = true;
+    for (int k = 0, item = blockIdx.x; ok; ++k) {
+      const DkvItem t = dkv_item(item, order, s, C::BMQ);
+      const int n = t.n_iter;
+      if (n > 0) {
+        // S^T of the item's first tile: its K block, Q(gt), and the softmax
+        // done reading the previous S^T
+        ok = wait(C::B_KFULL, ln) && wait(C::B_QFULL + gt % C::QST, gt / C::QST) &&
+             (gt == 0 || wait(C::B_SFREE, gt - 1));
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) issue_score(sbase + C::OFF_K, sbase + C::OFF_Q + (gt % C::QST) * C::TILE, C::S_COL);
+        if (leader) mma_commit(bar(C::B_SFULL));
+        if (n == 1 && leader) mma_commit(bar(C::B_KEMPTY));  // K read for the last time
+        // dP^T of the first tile (over the P^T / dS^T columns of the previous
+        // tile, whose MMAs precede it in issue order)
+        ok = wait(C::B_VFULL, ln) && wait(C::B_DOFULL + gt % C::DST, gt / C::DST);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) issue_score(sbase + C::OFF_V, sbase + C::OFF_DO + (gt % C::DST) * C::TILE, C::DP_COL);
+        if (leader) mma_commit(bar(C::B_DPFULL));
+        if (n == 1 && leader) mma_commit(bar(C::B_VEMPTY));
+        for (int it = 0; it < n; ++it) {
+          const int gi = gt + it;
+          const int qs = gi % C::QST, ds = gi % C::DST;
+          const bool more = it + 1 < n;
+          if (more) {
+            // next S^T as soon as the softmax has read this tile's S^T
+            const int nq = (gi + 1) % C::QST;
+            ok = wait(C::B_QFULL + nq, (gi + 1) / C::QST) && wait(C::B_SFREE, gi);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) issue_score(sbase + C::OFF_K, sbase + C::OFF_Q + nq * C::TILE, C::S_COL);
+            if (leader) mma_commit(bar(C::B_SFULL));
+            if (it + 2 == n && leader) mma_commit(bar(C::B_KEMPTY));
+          }
+          // P^T / dS^T of this tile in TMEM; for the item's first tile this
+          // also means the softmax warps have stored the previous item's dK, dV
+          ok = wait(C::B_PFULL, gi);
+          if (!ok) break;
+          tc_fence_after();
+          // dK += dS^T Q, then dV += P^T dO  (A from TMEM, B MN-major, K = query
+          // rows); each ring slot is released by the last MMA that reads it
+          const uint64_t qdesc = make_sdesc(sbase + C::OFF_Q + qs * C::TILE, C::REGION, 1024, 2);
+          const uint64_t ddesc = make_sdesc(sbase + C::OFF_DO + ds * C::TILE, C::REGION, 1024, 2);
+#pragma unroll
+          for (int kk = 0; kk < C::BMQ / 16; ++kk)
+            if (leader) mma_ts(tmem + C::DK_COL, tmem + C::dst_col(kk), qdesc + ((kk * 16 * 128) >> 4),
+                               idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          if (leader) mma_commit(bar(C::B_QEMPTY + qs));
+#pragma unroll
+          for (int kk = 0; kk < C::BMQ / 16; ++kk)
+            if (leader) mma_ts(tmem + C::DV_COL, tmem + C::pt_col(kk), ddesc + ((kk * 16 * 128) >> 4),
+                               idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          if (leader) mma_commit(bar(C::B_DOEMPTY + ds));
+          if (more) {
+            // dP^T(it+1) overwrites the P^T / dS^T columns the MMAs above read
+            // (tcgen05 MMAs of one thread execute in order)
+            const int nd = (gi + 1) % C::DST;
+            ok = wait(C::B_DOFULL + nd, (gi + 1) / C::DST);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) issue_score(sbase + C::OFF_V, sbase + C::OFF_DO + nd * C::TILE, C::DP_COL);
+            if (leader) mma_commit(bar(C::B_DPFULL));
+            if (it + 2 == n && leader) mma_commit(bar(C::B_VEMPTY));
+          }
+        }
+        if (!ok) break;
+        if (leader) mma_commit(bar(C::B_DONE));  // the item's dK, dV are final
+        gt += n;
+        ++ln;
+      }
+      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
     }
+    // every issued MMA completes before the CTA exits
+    if (leader) mma_commit(bar(C::B_DRAIN));
+    mbar_wait_poll(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
   } else if (warp == 3) {
     // ------------------------------------------- LSE / D-vector staging
-    for (int it = 0; it < n_iter; ++it) {
-      const int slot = it & 1;
-      const int h = g * reps + it / n_qt;
-      const int i0 = (i_lo + it % n_qt) * C::BMQ;
-      if (it >= 2)
-        mbar_wait(bar(C::B_STEMPTY + slot), ((it >> 1) - 1) & 1, tmo, abort_flag, wc.status);
-      float* dst = stats + slot * 2 * C::BMQ;
-      const int64_t base = static_cast<int64_t>(b * s.Hq + h) * s.Tq;
-      for (int t = lane; t < C::BMQ; t += 32) {
-        const int i = i0 + t;
-        float nl2 = -INFINITY, nd = 0.f;  // rows past Tq: P = 0
+    // a flat stream over the tiles of the CTA's items; each lane loads its
+    // four rows of the next tile into registers before waiting for that
+    // tile's slot, so the global-load latency hides behind the wait
+    int k = 0, item = blockIdx.x, it = 0;
+    DkvItem t = dkv_item(item, order, s, C::BMQ);
+    auto advance = [&]() {  // to the next tile with work; false at the end
+      while (it >= t.n_iter) {
+        if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) return false;
+        ++k;
+        t = dkv_item(item, order, s, C::BMQ);
+        it = 0;
+      }
+      return true;
+    };
+    constexpr int RPL = C::BMQ / 32;  // rows per lane
+    float L[RPL], Dv[RPL];
+    auto load = [&]() {
+      const int h = t.g * reps + it / t.n_qt;
+      const int i0 = (t.i_lo + it % t.n_qt) * C::BMQ;
+      const int64_t base = static_cast<int64_t>(t.b * s.Hq + h) * s.Tq;
+#pragma unroll
+      for (int r = 0; r < RPL; ++r) {
+        const int i = i0 + lane + 32 * r;
+        L[r] = -INFINITY;  // rows past Tq: P = 0
+        Dv[r] = 0.f;
         if (i < s.Tq) {
-          const float L = lse[base + i];
-          nl2 = (L == -INFINITY) ? -INFINITY : -L * kLog2e;  // row with no visible key: P = 0
-          nd = -dvec[base + i];
+          L[r] = lse[base + i];
+          Dv[r] = dvec[base + i];
         }
-        dst[t] = nl2;
-        dst[C::BMQ + t] = nd;
+      }
+    };
+    bool have = advance();
+    if (have) load();
+    for (int gt = 0; have; ++gt) {
+      const int slot = gt & 1;
+      if (gt >= 2 &&
+          !mbar_wait(bar(C::B_STEMPTY + slot), ((gt >> 1) - 1) & 1, tmo, abort_flag, wc.status))
+        break;
+      float* dst = stats + slot * 2 * C::BMQ;
+#pragma unroll
+      for (int r = 0; r < RPL; ++r) {
+        // -LSE * log2(e) (a row with no visible key: P = 0) and -D
+        dst[lane + 32 * r] = (L[r] == -INFINITY) ? -INFINITY : -L[r] * kLog2e;
+        dst[C::BMQ + lane + 32 * r] = -Dv[r];
       }
       mbar_arrive(bar(C::B_STFULL + slot));
+      ++it;
+      have = advance();
+      if (have) load();
     }
   } else if (warp >= 4) {
     // ------------------------------------------- softmax: P^T and dS^T
     const int wg = (warp - 4) >> 2;             // query columns [32 wg, 32 wg + 32)
     const int quarter = warp & 3;
-    const int krow = k0 + quarter * 32 + lane;  // KV row of this thread (TMEM lane)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint64_t c2 = f2_pack(s.scale_log2, s.scale_log2);
     const uint32_t col = C::DP_COL + wg * C::CW;  // this warpgroup's dP^T chunk
-    for (int it = 0; it < n_iter; ++it) {
-      const int slot = it & 1;
-      const int i0 = (i_lo + it % n_qt) * C::BMQ;
-      mbar_wait(bar(C::B_STFULL + slot), (it >> 1) & 1, tmo, abort_flag, wc.status);
-      mbar_wait(bar(C::B_SFULL), it & 1, tmo, abort_flag, wc.status);
-      tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld32(tmem + lane_base + C::S_COL + wg * C::CW, sv);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::B_SFREE));  // the next S^T may overwrite them
-      const float* nl_s = stats + slot * 2 * C::BMQ + wg * C::CW;  // -LSE * log2(e)
-      const float* nd_s = nl_s + C::BMQ;                           // -D
-      if (!block_unmasked(s, i0, i0 + C::BMQ, k0, k0 + kBM)) {
+    using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
+    int gt = 0, ln = 0;
+    bool ok = true;
+    for (int k = 0, item = blockIdx.x; ok; ++k) {
+      const DkvItem t = dkv_item(item, order, s, C::BMQ);
+      const int krow = t.k0 + quarter * 32 + lane;  // KV row of this thread (TMEM lane)
+      const int i_first = t.i_lo * C::BMQ, i_end = (t.i_lo + t.n_qt) * C::BMQ;
+      int i0 = i_first;  // query tile of this step: the heads of the group in turn
+      for (int it = 0; it < t.n_iter; ++it, i0 = (i0 + C::BMQ == i_end) ? i_first : i0 + C::BMQ) {
+        const int gi = gt + it;
+        const int slot = gi & 1;
+        ok = mbar_wait(bar(C::B_STFULL + slot), (gi >> 1) & 1, tmo, abort_flag, wc.status) &&
+             mbar_wait(bar(C::B_SFULL), gi & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_base + C::S_COL + wg * C::CW, sv);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_SFREE));  // the next S^T may overwrite them
+        const float* nl_s = stats + slot * 2 * C::BMQ + wg * C::CW;  // -LSE * log2(e)
+        const float* nd_s = nl_s + C::BMQ;                           // -D
+        if (!block_unmasked(s, i0, i0 + C::BMQ, t.k0, t.k0 + kBM)) {
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          if (!key_visible(i0 + wg * C::CW + q, krow, s.causal, s.window))
-            sv[q] = __float_as_uint(-INFINITY);
-      }
-      exp2_scores32(sv, c2, nl_s, true, 0);  // sv now holds P (fp32)
-      // dS^T = P^T o (dP^T - D) once dP^T(it) is in TMEM
-      mbar_wait(bar(C::B_DPFULL), it & 1, tmo, abort_flag, wc.status);
-      tc_fence_after();
-      uint32_t pv[32];
-      tmem_ld32(tmem + lane_base + col, pv);
-      tmem_ld_wait();
-      uint32_t pp[16], dsv[16];
+          for (int q = 0; q < 32; ++q)
+            if (!key_visible(i0 + wg * C::CW + q, krow, s.causal, s.window))
+              sv[q] = __float_as_uint(-INFINITY);
+        }
+        exp2_scores32(sv, c2, nl_s, true, 0);  // sv now holds P (fp32)
+        // dS^T = P^T o (dP^T - D) once dP^T(it) is in TMEM
+        ok = mbar_wait(bar(C::B_DPFULL), gi & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        tc_fence_after();
+        // two 16-column halves: load dP^T, then write [P^T | dS^T] over it
 #pragma unroll
-      for (int k = 0; k < 32; k += 4) {
-        const ulonglong2 nd = *reinterpret_cast<const ulonglong2*>(nd_s + k);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pv[16], w[16];
+          tmem_ld16(tmem + lane_base + col + 16 * h, pv);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          const uint64_t p2 = f2_pack(__uint_as_float(sv[k + e]), __uint_as_float(sv[k + e + 1]));
-          const uint64_t t = fadd2(
-              f2_pack(__uint_as_float(pv[k + e]), __uint_as_float(pv[k + e + 1])),
-              e == 0 ? nd.x : nd.y);
-          const float2 d2 = f2_unpack(fmul2(t, p2));
-          pp[(k + e) / 2] = pack2<C::BF16>(__uint_as_float(sv[k + e]), __uint_as_float(sv[k + e + 1]));
-          dsv[(k + e) / 2] = pack2<C::BF16>(d2.x, d2.y);
+          for (int k = 0; k < 16; k += 4) {
+            const ulonglong2 nd = *reinterpret_cast<const ulonglong2*>(nd_s + 16 * h + k);
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+              const int q = 16 * h + k + e;
+              const uint64_t p2 = f2_pack(__uint_as_float(sv[q]), __uint_as_float(sv[q + 1]));
+              const uint64_t d = fadd2(
+                  f2_pack(__uint_as_float(pv[k + e]), __uint_as_float(pv[k + e + 1])),
+                  e == 0 ? nd.x : nd.y);
+              const float2 d2 = f2_unpack(fmul2(d, p2));
+              w[(k + e) / 2] = pack2<C::BF16>(__uint_as_float(sv[q]), __uint_as_float(sv[q + 1]));
+              w[8 + (k + e) / 2] = pack2<C::BF16>(d2.x, d2.y);
+            }
+          }
+          tmem_st16(tmem + lane_base + col + 16 * h, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(C::B_PFULL));
+          mbar_arrive(bar(C::B_STEMPTY + slot));
         }
       }
-      tmem_st16(tmem + lane_base + col, pp);
-      tmem_st16(tmem + lane_base + col + 16, dsv);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(C::B_PFULL));
-        mbar_arrive(bar(C::B_STEMPTY + slot));
+      if (!ok) break;
+      // ----------------------------------------------------- item epilogue
+      // 16-column chunks of the dV then dK row (dK scaled), dealt round-robin
+      // over the softmax warpgroups; one row per thread. The accumulators are
+      // free again once every softmax warp has passed here (their next P/dS
+      // arrival orders it before the next item's first accumulating MMA).
+      const bool have = t.n_iter > 0;
+      if (have) {
+        ok = mbar_wait(bar(C::B_DONE), ln & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        tc_fence_after();
       }
-    }
-    // ------------------------------------------------------- epilogue
-    // 16-column chunks of the dV then dK row (dK scaled), dealt round-robin
-    // over the softmax warpgroups; one row per thread
-    if (n_iter > 0) {
-      mbar_wait(bar(C::B_DONE), 0, tmo, abort_flag, wc.status);
-      tc_fence_after();
-    }
-    using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
-    const bool valid = krow < s.Tkv;
-    const int64_t orow = (static_cast<int64_t>(bg) * s.Tkv + (valid ? krow : 0)) * C::D;
+      const bool valid = krow < s.Tkv;
+      const int64_t orow = (static_cast<int64_t>(t.bg) * s.Tkv + (valid ? krow : 0)) * C::D;
 #pragma unroll 1
-    for (int chunk = wg; chunk < 2 * C::D / 16; chunk += C::NWG) {
-      const bool is_dk = chunk >= C::D / 16;
-      const int cc = (is_dk ? chunk - C::D / 16 : chunk) * 16;
-      T16* dst = reinterpret_cast<T16*>(is_dk ? dk_out : dv_out) + orow + cc;
-      store_acc_chunk16<C::BF16>(tmem + lane_base + (is_dk ? C::DK_COL : C::DV_COL) + cc,
-                                 n_iter > 0, is_dk ? scale : 1.f, valid, dst);
+      for (int chunk = wg; chunk < 2 * C::D / 16; chunk += C::NWG) {
+        const bool is_dk = chunk >= C::D / 16;
+        const int cc = (is_dk ? chunk - C::D / 16 : chunk) * 16;
+        T16* dst = reinterpret_cast<T16*>(is_dk ? dk_out : dv_out) + orow + cc;
+        store_acc_chunk16<C::BF16>(tmem + lane_base + (is_dk ? C::DK_COL : C::DV_COL) + cc, have,
+                                   is_dk ? scale : 1.f, valid, dst);
+      }
+      if (have) {
+        tc_fence_before();
+        gt += t.n_iter;
+        ++ln;
+      }
+      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
     }
   }
 
@@ -393,6 +536,27 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 }
 
 // --------------------------------------------------------------------- dQ
+// One dQ work item: a (batch, head) and a block of 128 query rows; its tiles
+// are the key tiles the block sees.
+struct DqItem {
+  int bh, b, g, q0, j_lo, n_iter;
+};
+
+__device__ __forceinline__ DqItem dq_item(int linear, const TileOrder& o, const AttnShape& s,
+                                          int bn) {
+  DqItem t;
+  int qt;
+  decode_tile(linear, o, &t.bh, &qt);
+  t.b = t.bh / s.Hq;
+  t.g = (t.bh - t.b * s.Hq) / (s.Hq / s.Hkv);
+  t.q0 = qt * kBM;
+  int kf, kl;
+  key_range(s, t.q0, min(s.Tq, t.q0 + kBM), &kf, &kl);
+  t.j_lo = kf / bn;
+  t.n_iter = max(0, (kl + bn - 1) / bn - t.j_lo);
+  return t;
+}
+
 template <int D_, bool BF16_, int NWG_>
 struct DqCfg {
   static constexpr int D = D_;
@@ -411,24 +575,30 @@ struct DqCfg {
   static constexpr int OFF_K = OFF_DO + TILE;
   static constexpr int OFF_V = OFF_K + KST * TILE;
   static constexpr int OFF_BAR = OFF_V + VST * TILE;
-  // barriers: q_full, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST],
-  // s_full, s_free, dp_full, p_full, done
-  static constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + KST,
-                       B_VFULL = B_KEMPTY + KST, B_VEMPTY = B_VFULL + VST,
-                       B_SFULL = B_VEMPTY + VST, B_SFREE = B_SFULL + 1, B_DPFULL = B_SFULL + 2,
-                       B_PFULL = B_SFULL + 3, B_DONE = B_SFULL + 4, NBAR = B_DONE + 1;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  // barriers: q_full, q_empty, do_full, do_empty, k_full[KST], k_empty[KST],
+  // v_full[VST], v_empty[VST], s_full, s_free, dp_full, p_full, done[2],
+  // acc_free[2], drain
+  static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_DOFULL = 2, B_DOEMPTY = 3, B_KFULL = 4,
+                       B_KEMPTY = B_KFULL + KST, B_VFULL = B_KEMPTY + KST,
+                       B_VEMPTY = B_VFULL + VST, B_SFULL = B_VEMPTY + VST,
+                       B_SFREE = B_SFULL + 1, B_DPFULL = B_SFULL + 2, B_PFULL = B_SFULL + 3,
+                       B_DONE = B_SFULL + 4, B_ACCFREE = B_DONE + 2, B_DRAIN = B_ACCFREE + 2,
+                       B_CLCFULL = B_DRAIN + 1, B_CLCEMPTY = B_CLCFULL + kClcSlots,
+                       NBAR = B_CLCEMPTY + kClcSlots;
+  static constexpr int OFF_CLC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // item responses
+  static constexpr int OFF_MISC = OFF_CLC + 16 * kClcSlots;
   static constexpr int SMEM_BYTES = OFF_MISC + 16;  // base must be 1024-aligned (checked)
   static constexpr int THREADS = 128 + 128 * NWG;
   static constexpr int S_COL = 0;
   static constexpr int DP_COL = 128;
-  static constexpr int DQ_COL = 256;
+  static constexpr int DQ_COL = 256;  // two accumulators, 128 columns apart
   static constexpr uint32_t ds_col(int kk) { return chunk_operand_col(DP_COL, kk); }
   static_assert(NWG == 4, "one 32-column chunk per softmax warpgroup");
-  static_assert(D <= 128, "dQ accumulator in TMEM columns 256-383");
+  static_assert(D <= 128, "dQ accumulators in TMEM columns 256-383 and 384-511");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
+// Persistent like the dK/dV kernel above.
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
 fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -448,21 +618,17 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const uint64_t tmo = wc.timeout_cycles;
-
-  int bh, qt;  // (b * Hq + h, block of 128 query rows)
-  decode_tile(blockIdx.x, order, &bh, &qt);
-  const int b = bh / s.Hq, h = bh % s.Hq;
-  const int g = h / (s.Hq / s.Hkv);
-  const int q0 = qt * kBM;
-  int kf, kl;
-  key_range(s, q0, min(s.Tq, q0 + kBM), &kf, &kl);
-  const int j_lo = kf / C::BN;
-  const int n_iter = max(0, (kl + C::BN - 1) / C::BN - j_lo);
+  const ItemQueue iq{sbase + C::OFF_CLC, bar(C::B_CLCFULL), bar(C::B_CLCEMPTY)};
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < C::NBAR; ++i)  // one arrival per softmax warp on p_full / s_free
-      mbar_init(bar(i), (i == C::B_PFULL || i == C::B_SFREE) ? 4u * C::NWG : 1u);
+    for (int i = 0; i < C::NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i == C::B_PFULL || i == C::B_SFREE || i == C::B_ACCFREE || i == C::B_ACCFREE + 1)
+        cnt = 4 * C::NWG;  // one arrival per softmax warp
+      if (i >= C::B_CLCEMPTY && i < C::B_CLCEMPTY + kClcSlots) cnt = C::THREADS / 32;
+      mbar_init(bar(i), cnt);
+    }
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -474,167 +640,274 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 || warp == 2) {
-    // producers: warp 0 loads Q, dO once, then the K ring; warp 2 the V ring,
-    // each refilled the moment its own slot frees
-    if (n_iter > 0) {
-      // the whole warp runs the loop (a lone active lane whose siblings wait at
-      // the final barrier issues far slower); one elected lane issues
-      const bool leader = elect_one_sync();
-      const bool k_ring = warp == 0;
-      if (k_ring) {
-        if (leader) tma_prefetch_desc(&map_k);
-        if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE);
-        for (int r = 0; r < C::KREG; ++r) {
-          if (leader) tma_load_3d(sbase + C::OFF_Q + r * C::REGION, &map_q, bar(C::B_QFULL), r * 64, q0, bh);
-          if (leader) tma_load_3d(sbase + C::OFF_DO + r * C::REGION, &map_do, bar(C::B_QFULL), r * 64, q0, bh);
-        }
-      } else if (leader) {
-        tma_prefetch_desc(&map_v);
+  if (warp == 3) {
+    // ------------------------------------------------ producer: Q and dO
+    // once per item, each as soon as the previous item's last MMA reading it
+    // (its last S, its last dP) completes
+    const bool leader = elect_one_sync();
+    int ln = 0, nq = 0, ndo = 0;  // items with work; Q, dO loads issued
+    bool ok = true;
+    for (int k = 0, item = blockIdx.x; ok; ++k) {
+      const DqItem t = dq_item(item, order, s, C::BN);
+      if (t.n_iter > 0) {
+        if (ln > 0) ok = mbar_wait_poll(bar(C::B_QEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE);
+        for (int r = 0; r < C::KREG; ++r)
+          if (leader) tma_load_3d(sbase + C::OFF_Q + r * C::REGION, &map_q, bar(C::B_QFULL), r * 64, t.q0, t.bh);
+        ++nq;
+        if (ln > 0) ok = mbar_wait_poll(bar(C::B_DOEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        if (leader) mbar_arrive_expect_tx(bar(C::B_DOFULL), C::TILE);
+        for (int r = 0; r < C::KREG; ++r)
+          if (leader) tma_load_3d(sbase + C::OFF_DO + r * C::REGION, &map_do, bar(C::B_DOFULL), r * 64, t.q0, t.bh);
+        ++ndo;
+        ++ln;
       }
-      const int zkv = b * s.Hkv + g;
-      const int nst = k_ring ? C::KST : C::VST;
-      const int full = k_ring ? C::B_KFULL : C::B_VFULL, empty = k_ring ? C::B_KEMPTY : C::B_VEMPTY;
-      const uint32_t ring = sbase + (k_ring ? C::OFF_K : C::OFF_V);
-      const CUtensorMap* map = k_ring ? &map_k : &map_v;
-      for (int it = 0; it < n_iter; ++it) {
-        const int kr = (j_lo + it) * C::BN;
-        const int st = it % nst;
-        if (it >= nst)
-          mbar_wait_poll(bar(empty + st), ((it / nst) - 1) & 1, tmo, abort_flag, wc.status);
+      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
+    }
+    if (*abort_flag) {
+      drain_ring(bar(C::B_QFULL), 1, nq, tmo, wc.status);
+      drain_ring(bar(C::B_DOFULL), 1, ndo, tmo, wc.status);
+    }
+  } else if (warp == 0 || warp == 2) {
+    // ------------------------------------------- producers: K ring, V ring
+    // each refilled the moment its own slot frees (warp 0 also requests the
+    // items); the whole warp runs the loop, one elected lane issues
+    const bool leader = elect_one_sync();
+    const bool k_ring = warp == 0;
+    if (leader) tma_prefetch_desc(k_ring ? &map_k : &map_v);
+    const int nst = k_ring ? C::KST : C::VST;
+    const int full = k_ring ? C::B_KFULL : C::B_VFULL, empty = k_ring ? C::B_KEMPTY : C::B_VEMPTY;
+    const uint32_t ring = sbase + (k_ring ? C::OFF_K : C::OFF_V);
+    const CUtensorMap* map = k_ring ? &map_k : &map_v;
+    int gt = 0, asked = 0;
+    bool ok = true;
+    for (int k = 0, item = blockIdx.x; ok; ++k) {
+      if (k_ring) {
+        ok = clc_request(iq, k, leader, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        ++asked;
+      }
+      const DqItem t = dq_item(item, order, s, C::BN);
+      const int zkv = t.b * s.Hkv + t.g;
+      for (int it = 0; it < t.n_iter; ++it, ++gt) {
+        const int kr = (t.j_lo + it) * C::BN;
+        const int st = gt % nst;
+        if (gt >= nst) ok = mbar_wait_poll(bar(empty + st), ((gt / nst) - 1) & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
         if (leader) mbar_arrive_expect_tx(bar(full + st), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
           if (leader) tma_load_3d(ring + st * C::TILE + r * C::REGION, map, bar(full + st), r * 64, kr, zkv);
       }
+      if (!ok) break;
+      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
+    }
+    if (*abort_flag) {
+      drain_ring(bar(full), nst, gt, tmo, wc.status);
+      if (k_ring) drain_ring(iq.full, kClcSlots, asked, tmo, wc.status);
     }
   } else if (warp == 1) {
-    if (n_iter > 0) {
-      // the whole warp runs the loop (a lone active lane whose siblings wait at
-      // the final barrier issues far slower); one elected lane issues
-      const bool leader = elect_one_sync();
-      constexpr uint32_t ab = C::BF16 ? 1 : 0;
-      constexpr uint32_t idesc_s = make_idesc_f16(kBM, C::BN, ab, 0, 0);
-      constexpr uint32_t idesc_q = make_idesc_f16(kBM, C::D, ab, 0, 1);
-      auto issue_score = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
-        const uint64_t ad = make_sdesc(a_base, 16, 1024, 2), bd = make_sdesc(b_base, 16, 1024, 2);
+    // ----------------------------------------------------------- MMA issuer
+    const bool leader = elect_one_sync();
+    constexpr uint32_t ab = C::BF16 ? 1 : 0;
+    constexpr uint32_t idesc_s = make_idesc_f16(kBM, C::BN, ab, 0, 0);
+    constexpr uint32_t idesc_q = make_idesc_f16(kBM, C::D, ab, 0, 1);
+    auto issue_score = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
+      const uint64_t ad = make_sdesc(a_base, 16, 1024, 2), bd = make_sdesc(b_base, 16, 1024, 2);
 #pragma unroll
-        for (int kk = 0; kk < C::D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::REGION + (kk & 3) * 32;
-          if (leader) mma_ss(tmem + col, ad + (off >> 4), bd + (off >> 4), idesc_s, kk > 0);
-        }
-      };
-      mbar_wait_poll(bar(C::B_QFULL), 0, tmo, abort_flag, wc.status);
-      mbar_wait_poll(bar(C::B_KFULL + 0), 0, tmo, abort_flag, wc.status);
-      tc_fence_after();
-      if (leader) issue_score(sbase + C::OFF_Q, sbase + C::OFF_K, C::S_COL);
-      if (leader) mma_commit(bar(C::B_SFULL));
-      mbar_wait_poll(bar(C::B_VFULL + 0), 0, tmo, abort_flag, wc.status);
-      tc_fence_after();
-      if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V, C::DP_COL);
-      if (leader) mma_commit(bar(C::B_DPFULL));
-      if (leader) mma_commit(bar(C::B_VEMPTY + 0));
-      for (int it = 0; it < n_iter; ++it) {
-        const int ks = it % C::KST;
-        const bool more = it + 1 < n_iter;
-        if (more) {
-          const int nk = (it + 1) % C::KST;
-          mbar_wait_poll(bar(C::B_KFULL + nk), ((it + 1) / C::KST) & 1, tmo, abort_flag, wc.status);
-          mbar_wait_poll(bar(C::B_SFREE), it & 1, tmo, abort_flag, wc.status);
-          tc_fence_after();
-          if (leader) issue_score(sbase + C::OFF_Q, sbase + C::OFF_K + nk * C::TILE, C::S_COL);
-          if (leader) mma_commit(bar(C::B_SFULL));
-        }
-        mbar_wait_poll(bar(C::B_PFULL), it & 1, tmo, abort_flag, wc.status);
-        tc_fence_after();
-        // dQ += dS K   (dS from TMEM, K as MN-major B, K = key rows)
-        const uint64_t kdesc = make_sdesc(sbase + C::OFF_K + ks * C::TILE, C::REGION, 1024, 2);
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          if (leader) mma_ts(tmem + C::DQ_COL, tmem + C::ds_col(kk), kdesc + ((kk * 16 * 128) >> 4), idesc_q,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        if (leader) mma_commit(bar(C::B_KEMPTY + ks));
-        if (more) {
-          // dP(it+1) overwrites the dS columns the MMAs above read (in order)
-          const int nv = (it + 1) % C::VST;
-          mbar_wait_poll(bar(C::B_VFULL + nv), ((it + 1) / C::VST) & 1, tmo, abort_flag, wc.status);
-          tc_fence_after();
-          if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V + nv * C::TILE, C::DP_COL);
-          if (leader) mma_commit(bar(C::B_DPFULL));
-          if (leader) mma_commit(bar(C::B_VEMPTY + nv));  // V is read by dP only
-        }
+      for (int kk = 0; kk < C::D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::REGION + (kk & 3) * 32;
+        if (leader) mma_ss(tmem + col, ad + (off >> 4), bd + (off >> 4), idesc_s, kk > 0);
       }
-      if (leader) mma_commit(bar(C::B_DONE));
-      mbar_wait_poll(bar(C::B_DONE), 0, tmo, nullptr, wc.status);
+    };
+    auto wait = [&](int b, int parity) {
+      return mbar_wait_poll(bar(b), parity & 1, tmo, abort_flag, wc.status);
+    };
+    int gt = 0, ln = 0;
+    bool ok = true;
+    for (int k = 0, item = blockIdx.x; ok; ++k) {
+      const DqItem t = dq_item(item, order, s, C::BN);
+      const int n = t.n_iter;
+      if (n > 0) {
+        const int buf = ln & 1;
+        const uint32_t dq_col = C::DQ_COL + 128 * buf;
+        // S of the item's first tile: its Q, K(gt), and the softmax done
+        // reading the previous S
+        ok = wait(C::B_QFULL, ln) && wait(C::B_KFULL + gt % C::KST, gt / C::KST) &&
+             (gt == 0 || wait(C::B_SFREE, gt - 1));
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) issue_score(sbase + C::OFF_Q, sbase + C::OFF_K + (gt % C::KST) * C::TILE, C::S_COL);
+        if (leader) mma_commit(bar(C::B_SFULL));
+        if (n == 1 && leader) mma_commit(bar(C::B_QEMPTY));  // Q read for the last time
+        // dP of the first tile (over the dS columns of the previous tile, whose
+        // dQ MMAs precede it in issue order)
+        ok = wait(C::B_DOFULL, ln) && wait(C::B_VFULL + gt % C::VST, gt / C::VST);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V + (gt % C::VST) * C::TILE, C::DP_COL);
+        if (leader) mma_commit(bar(C::B_DPFULL));
+        if (leader) mma_commit(bar(C::B_VEMPTY + gt % C::VST));  // V is read by dP only
+        if (n == 1 && leader) mma_commit(bar(C::B_DOEMPTY));
+        // this accumulator's previous item has been stored
+        if (ln >= 2) ok = wait(C::B_ACCFREE + buf, (ln >> 1) - 1);
+        if (!ok) break;
+        for (int it = 0; it < n; ++it) {
+          const int gi = gt + it;
+          const int ks = gi % C::KST;
+          const bool more = it + 1 < n;
+          if (more) {
+            const int nk = (gi + 1) % C::KST;
+            ok = wait(C::B_KFULL + nk, (gi + 1) / C::KST) && wait(C::B_SFREE, gi);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) issue_score(sbase + C::OFF_Q, sbase + C::OFF_K + nk * C::TILE, C::S_COL);
+            if (leader) mma_commit(bar(C::B_SFULL));
+            if (it + 2 == n && leader) mma_commit(bar(C::B_QEMPTY));
+          }
+          ok = wait(C::B_PFULL, gi);
+          if (!ok) break;
+          tc_fence_after();
+          // dQ += dS K   (dS from TMEM, K as MN-major B, K = key rows)
+          const uint64_t kdesc = make_sdesc(sbase + C::OFF_K + ks * C::TILE, C::REGION, 1024, 2);
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            if (leader) mma_ts(tmem + dq_col, tmem + C::ds_col(kk), kdesc + ((kk * 16 * 128) >> 4), idesc_q,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+          if (leader) mma_commit(bar(C::B_KEMPTY + ks));
+          if (more) {
+            // dP(it+1) overwrites the dS columns the MMAs above read (in order)
+            const int nv = (gi + 1) % C::VST;
+            ok = wait(C::B_VFULL + nv, (gi + 1) / C::VST);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V + nv * C::TILE, C::DP_COL);
+            if (leader) mma_commit(bar(C::B_DPFULL));
+            if (leader) mma_commit(bar(C::B_VEMPTY + nv));
+            if (it + 2 == n && leader) mma_commit(bar(C::B_DOEMPTY));
+          }
+        }
+        if (!ok) break;
+        if (leader) mma_commit(bar(C::B_DONE + buf));  // this item's dQ is final
+        gt += n;
+        ++ln;
+      }
+      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
     }
+    // every issued MMA completes before the CTA exits
+    if (leader) mma_commit(bar(C::B_DRAIN));
+    mbar_wait_poll(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
   } else if (warp >= 4) {
     const int wg = (warp - 4) >> 2;  // key columns [32 wg, 32 wg + 32)
     const int quarter = warp & 3;
-    const int row = q0 + quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    float nl2 = -INFINITY, nd = 0.f;  // -LSE * log2(e) and -D of this row
-    if (row < s.Tq) {
-      const int64_t idx = static_cast<int64_t>(bh) * s.Tq + row;
-      const float L = lse[idx];
-      nl2 = (L == -INFINITY) ? -INFINITY : -L * kLog2e;  // no visible key: P = 0
-      nd = -dvec[idx];
-    }
-    const uint64_t c2 = f2_pack(s.scale_log2, s.scale_log2), nl2x2 = f2_pack(nl2, nl2),
-                   ndx2 = f2_pack(nd, nd);
+    const uint64_t c2 = f2_pack(s.scale_log2, s.scale_log2);
     const uint32_t col = C::DP_COL + wg * C::CW;
-    for (int it = 0; it < n_iter; ++it) {
-      const int kb = (j_lo + it) * C::BN + wg * C::CW;
-      mbar_wait(bar(C::B_SFULL), it & 1, tmo, abort_flag, wc.status);
-      tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld32(tmem + lane_base + C::S_COL + wg * C::CW, sv);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::B_SFREE));  // the next S may overwrite them
-      if (!block_unmasked(s, q0, q0 + kBM, kb, kb + C::CW)) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int j = kb + k;
-          if (j >= s.Tkv || !key_visible(row, j, s.causal, s.window))
-            sv[k] = __float_as_uint(-INFINITY);
-        }
-      }
-      exp2_scores32(sv, c2, nullptr, false, nl2x2);  // sv now holds P (fp32)
-      mbar_wait(bar(C::B_DPFULL), it & 1, tmo, abort_flag, wc.status);
-      tc_fence_after();
-      uint32_t pv[32];
-      tmem_ld32(tmem + lane_base + col, pv);
-      tmem_ld_wait();
-      uint32_t dsv[16];
-#pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        // ds = p * (dp - D)
-        const uint64_t t =
-            fadd2(f2_pack(__uint_as_float(pv[k]), __uint_as_float(pv[k + 1])), ndx2);
-        const float2 d2 = f2_unpack(
-            fmul2(t, f2_pack(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1]))));
-        dsv[k / 2] = pack2<C::BF16>(d2.x, d2.y);
-      }
-      tmem_st16(tmem + lane_base + col, dsv);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::B_PFULL));
-    }
-    // epilogue: 16-column chunks of the dQ row dealt round-robin over the
-    // softmax warpgroups
-    if (n_iter > 0) {
-      mbar_wait(bar(C::B_DONE), 0, tmo, abort_flag, wc.status);
-      tc_fence_after();
-    }
     using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
-    const bool valid = row < s.Tq;
-    T16* dst_row = reinterpret_cast<T16*>(dq_out) +
-                   (static_cast<int64_t>(bh) * s.Tq + (valid ? row : 0)) * C::D;
+    // LSE and D of this thread's row of an item (loaded one item ahead)
+    auto row_stats = [&](const DqItem& u, float* L, float* dv) {
+      *L = -INFINITY;
+      *dv = 0.f;
+      const int r = u.q0 + quarter * 32 + lane;
+      if (u.n_iter > 0 && r < s.Tq) {
+        const int64_t idx = static_cast<int64_t>(u.bh) * s.Tq + r;
+        *L = lse[idx];
+        *dv = dvec[idx];
+      }
+    };
+    DqItem t = dq_item(blockIdx.x, order, s, C::BN);
+    float L, dv;
+    row_stats(t, &L, &dv);
+    int gt = 0, ln = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int row = t.q0 + quarter * 32 + lane;
+      // -LSE * log2(e) and -D of this row; no visible key (or past Tq): P = 0
+      const float nl2 = (L == -INFINITY) ? -INFINITY : -L * kLog2e;
+      const uint64_t nl2x2 = f2_pack(nl2, nl2), ndx2 = f2_pack(-dv, -dv);
+      for (int it = 0; it < t.n_iter; ++it) {
+        const int gi = gt + it;
+        const int kb = (t.j_lo + it) * C::BN + wg * C::CW;
+        ok = mbar_wait(bar(C::B_SFULL), gi & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_base + C::S_COL + wg * C::CW, sv);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_SFREE));  // the next S may overwrite them
+        if (!block_unmasked(s, t.q0, t.q0 + kBM, kb, kb + C::CW)) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int j = kb + q;
+            if (j >= s.Tkv || !key_visible(row, j, s.causal, s.window))
+              sv[q] = __float_as_uint(-INFINITY);
+          }
+        }
+        exp2_scores32(sv, c2, nullptr, false, nl2x2);  // sv now holds P (fp32)
+        ok = mbar_wait(bar(C::B_DPFULL), gi & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t pv[32];
+        tmem_ld32(tmem + lane_base + col, pv);
+        tmem_ld_wait();
+        uint32_t dsv[16];
+#pragma unroll
+        for (int q = 0; q < 32; q += 2) {
+          // ds = p * (dp - D)
+          const uint64_t d =
+              fadd2(f2_pack(__uint_as_float(pv[q]), __uint_as_float(pv[q + 1])), ndx2);
+          const float2 d2 = f2_unpack(
+              fmul2(d, f2_pack(__uint_as_float(sv[q]), __uint_as_float(sv[q + 1]))));
+          dsv[q / 2] = pack2<C::BF16>(d2.x, d2.y);
+        }
+        tmem_st16(tmem + lane_base + col, dsv);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_PFULL));
+      }
+      if (!ok) break;
+      // the next item and its row statistics, loaded while this one is stored
+      int next = 0;
+      const bool more = clc_next(iq, k, lane, &next, tmo, abort_flag, wc.status);
+      DqItem tn = t;
+      float Ln = -INFINITY, dvn = 0.f;
+      if (more) {
+        tn = dq_item(next, order, s, C::BN);
+        row_stats(tn, &Ln, &dvn);
+      }
+      // ----------------------------------------------------- item epilogue
+      // 16-column chunks of the dQ row dealt round-robin over the softmax
+      // warpgroups; then the accumulator is free for the item after next
+      const bool have = t.n_iter > 0;
+      const int buf = ln & 1;
+      if (have) {
+        ok = mbar_wait(bar(C::B_DONE + buf), (ln >> 1) & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const bool valid = row < s.Tq;
+      T16* dst_row = reinterpret_cast<T16*>(dq_out) +
+                     (static_cast<int64_t>(t.bh) * s.Tq + (valid ? row : 0)) * C::D;
 #pragma unroll 1
-    for (int chunk = wg; chunk < C::D / 16; chunk += C::NWG)
-      store_acc_chunk16<C::BF16>(tmem + lane_base + C::DQ_COL + chunk * 16, n_iter > 0, scale,
-                                 valid, dst_row + chunk * 16);
+      for (int chunk = wg; chunk < C::D / 16; chunk += C::NWG)
+        store_acc_chunk16<C::BF16>(tmem + lane_base + C::DQ_COL + 128 * buf + chunk * 16, have, scale,
+                                   valid, dst_row + chunk * 16);
+      if (have) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_ACCFREE + buf));
+        gt += t.n_iter;
+        ++ln;
+      }
+      if (!more) break;
+      t = tn;
+      L = Ln;
+      dv = dvn;
+    }
   }
 
   tc_fence_before();

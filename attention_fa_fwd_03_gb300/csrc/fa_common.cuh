@@ -52,6 +52,48 @@ __device__ __forceinline__ void decode_tile(int linear, const TileOrder& o, int*
   *tile = o.heavy_last ? o.tiles - 1 - t : t;
 }
 
+// Work items of a persistent CTA, handed out by cluster launch control: the
+// CTA starts on item blockIdx.x and, instead of exiting after it, takes over
+// the next CTA of the grid that has not started yet (in launch order, so the
+// TileOrder is kept and faster SMs take more items). Warp 0 requests the
+// response that names item k + 1 when it starts item k; every warp reads it
+// once done with item k. Responses rotate through kClcSlots slots.
+constexpr int kClcSlots = 4;
+
+struct ItemQueue {
+  uint32_t resp;   // kClcSlots responses of 16 bytes (shared address, 16-byte aligned)
+  uint32_t full;   // kClcSlots barriers: arrival count 1, plus 16 transaction bytes
+  uint32_t empty;  // kClcSlots barriers: arrival count = warps of the CTA
+};
+
+// Warp 0, whole warp: request the response for item k + 1 once slot k % S has
+// been read by every warp (for item k + 1 - S).
+__device__ __forceinline__ bool clc_request(const ItemQueue& q, int k, bool leader, uint64_t tmo,
+                                            volatile int* abort, uint32_t* status) {
+  const int slot = k % kClcSlots;
+  if (k >= kClcSlots &&
+      !mbar_wait_poll(q.empty + 8u * slot, ((k / kClcSlots) - 1) & 1, tmo, abort, status))
+    return false;
+  if (leader) {
+    mbar_arrive_expect_tx(q.full + 8u * slot, 16);
+    clc_try_cancel(q.resp + 16u * slot, q.full + 8u * slot);
+  }
+  __syncwarp();
+  return true;
+}
+
+// Every warp, done with item k: the next item in *item, or false when the
+// grid has none left (or a wait gave up).
+__device__ __forceinline__ bool clc_next(const ItemQueue& q, int k, int lane, int* item,
+                                         uint64_t tmo, volatile int* abort, uint32_t* status) {
+  const int slot = k % kClcSlots;
+  if (!mbar_wait(q.full + 8u * slot, (k / kClcSlots) & 1, tmo, abort, status)) return false;
+  const bool got = clc_query(q.resp + 16u * slot, item);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(q.empty + 8u * slot);
+  return got;
+}
+
 __host__ __device__ __forceinline__ bool key_visible(int i, int j, int causal, int window) {
   if (causal && j > i) return false;
   if (window > 0 && i >= j && i - j >= window) return false;

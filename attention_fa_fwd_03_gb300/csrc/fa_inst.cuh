@@ -15,8 +15,7 @@ namespace fa {
 // per-tile operands and outputs pass through it too), rounded to a multiple
 // of `align` units.
 inline TileOrder make_order(int units, int tiles, int64_t shared_bytes_per_unit, int align,
-                            bool heavy_last) {
-  const int64_t target = int64_t(32) << 20;
+                            bool heavy_last, int64_t target = int64_t(32) << 20) {
   int64_t chunk = target / (shared_bytes_per_unit > 0 ? shared_bytes_per_unit : 1);
   chunk = chunk / align * align;
   if (chunk < align) chunk = align;
@@ -37,11 +36,17 @@ inline TileOrder query_block_order(const AttnShape& s, int rows_per_block, int D
                     reps, s.causal != 0);
 }
 
+// KV-row blocks of one group share its reps heads' Q and dO. The dK/dV kernel
+// nevertheless runs best as one chunk over all groups (measured on the
+// causal B4 Hq32 Hkv8 T4096 D128 shape: 0.71 ms against 0.81 ms with 32 MiB
+// chunks): heaviest blocks first over the whole grid balances the SMs, and
+// its tile loads are latency-bound rather than limited by L2 misses.
+constexpr int64_t kDkvChunkBytes = int64_t(1) << 40;
 // KV-row blocks of one group share its reps heads' Q and dO.
 inline TileOrder kv_block_order(const AttnShape& s, int D) {
   const int reps = s.Hq / s.Hkv;
   const int64_t qdo_bytes = int64_t(reps) * s.Tq * D * 2 * 2;
-  return make_order(s.B * s.Hkv, (s.Tkv + kBM - 1) / kBM, qdo_bytes, 1, false);
+  return make_order(s.B * s.Hkv, (s.Tkv + kBM - 1) / kBM, qdo_bytes, 1, false, kDkvChunkBytes);
 }
 
 template <class C>

@@ -174,6 +174,36 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// ------------------------------------------------- cluster launch control
+// Dynamic scheduling for persistent CTAs: a running CTA asks the hardware to
+// cancel the launch of a CTA of its grid that has not started yet and takes
+// over that CTA's work. The 16-byte response lands in shared memory at
+// `resp` (16-byte aligned) and completes `bar` with 16 transaction bytes.
+// Issued by one thread; not again once a response reported failure.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
+      " [%0], [%1];" ::"r"(resp), "r"(bar)
+      : "memory");
+}
+
+// Decode a response: true, with the x index of the cancelled CTA, when a CTA
+// was cancelled; false when the grid had none left to give.
+__device__ __forceinline__ bool clc_query(uint32_t resp, int* ctaid_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n .reg .b128 r;\n .reg .pred p;\n"
+      " ld.shared.b128 r, [%2];\n"
+      " clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      " clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n}"
+      : "=r"(ok), "=r"(x)
+      : "r"(resp)
+      : "memory");
+  *ctaid_x = static_cast<int>(x);
+  return ok != 0;
+}
+
 // ------------------------------------------------------------------ tcgen05
 // TMEM allocation: executed by one full warp. The allocated base address is
 // written to the shared-memory word at `dst`.

@@ -75,8 +75,8 @@ def load_peaks() -> dict:
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cuh"],
     "fa_bwd_dvec_kernel": ["fa_bwd.cuh"],
-    "fa_bwd_dkv_kernel": ["fa_bwd.cuh"],
-    "fa_bwd_dq_kernel": ["fa_bwd.cuh"],
+    "fa_bwd_dkv_kernel": ["fa_bwd_pipelined.cuh", "fa_bwd.cuh"],
+    "fa_bwd_dq_kernel": ["fa_bwd_pipelined.cuh", "fa_bwd.cuh"],
 }
 COMMON_SOURCES = ["fa_common.cuh", "sm103_ptx.cuh", "fa_inst.cuh", "fa_inst_d64.cu",
                   "fa_inst_d96.cu", "fa_inst_d128.cu", "fa_inst_d256.cu"]
