@@ -55,27 +55,63 @@ __host__ __device__ constexpr uint32_t chunk_operand_col(uint32_t dp_col, int kk
   return dp_col + 32 * (kk >> 1) + 8 * (kk & 1);
 }
 
-// Store one 16-column chunk of an fp32 TMEM accumulator row, scaled, as
-// 16-bit values (32 bytes of the output row).
-template <bool BF16, class T16>
-__device__ __forceinline__ void store_acc_chunk16(uint32_t taddr, bool have_data, float mul,
-                                                  bool valid, T16* dst) {
-  uint32_t v[16];
-  if (have_data) {
-    tmem_ld16(taddr, v);
-    tmem_ld_wait();
-  }
-  uint32_t w[8];
+// Store a 32-row x 8S-column block of an fp32 TMEM accumulator (the warp's
+// TMEM lane quarter, columns [taddr, taddr + 8S)), scaled by `mul`, as 16-bit
+// values to rows [0, rows_valid) of `base` (row r at base + r * ld). A thread
+// holds one row, so storing it directly would make every 16-byte store of the
+// warp touch 32 rows; instead the lanes first transpose 16-byte segments
+// within groups of S lanes (log2 S butterfly exchange steps), after which each
+// store instruction writes 32 / S whole 16S-byte row segments.
+template <int S, bool BF16, class T16>
+__device__ __forceinline__ void store_acc_block(uint32_t taddr, bool have_data, float mul,
+                                                T16* base, int64_t ld, int rows_valid) {
+  static_assert(S == 4 || S == 8, "segments per row");
+  const int lane = threadIdx.x & 31;
+  uint4 a[S];  // this lane's row: S segments of 8 values
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float a = have_data ? __uint_as_float(v[2 * k]) * mul : 0.f;
-    const float b = have_data ? __uint_as_float(v[2 * k + 1]) * mul : 0.f;
-    w[k] = pack2<BF16>(a, b);
+  for (int h = 0; h < S / 2; ++h) {
+    uint32_t v[16];
+    if (have_data) {
+      tmem_ld16(taddr + 16 * h, v);
+      tmem_ld_wait();
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = have_data ? __uint_as_float(v[8 * q + 2 * e]) * mul : 0.f;
+        const float y = have_data ? __uint_as_float(v[8 * q + 2 * e + 1]) * mul : 0.f;
+        w[e] = pack2<BF16>(x, y);
+      }
+      a[2 * h + q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
   }
-  if (valid) {
-    uint4* d = reinterpret_cast<uint4*>(dst);
-    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  // after the exchange, lane c of a group holds in a[j] segment c of the
+  // group's row j
+#pragma unroll
+  for (int k = S / 2; k >= 1; k >>= 1) {
+    const bool hi = (lane & k) != 0;
+#pragma unroll
+    for (int e = 0; e < S; ++e) {
+      if (e & k) continue;
+      const uint4 send = hi ? a[e] : a[e ^ k];
+      uint4 r;
+      r.x = __shfl_xor_sync(0xffffffffu, send.x, k);
+      r.y = __shfl_xor_sync(0xffffffffu, send.y, k);
+      r.z = __shfl_xor_sync(0xffffffffu, send.z, k);
+      r.w = __shfl_xor_sync(0xffffffffu, send.w, k);
+      if (hi)
+        a[e] = r;
+      else
+        a[e ^ k] = r;
+    }
+  }
+  const int g = lane / S, c = lane % S;
+#pragma unroll
+  for (int j = 0; j < S; ++j) {
+    const int r = S * g + j;
+    if (r < rows_valid) *reinterpret_cast<uint4*>(base + r * ld + 8 * c) = a[j];
   }
 }
 
@@ -508,15 +544,19 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (!ok) break;
         tc_fence_after();
       }
-      const bool valid = krow < s.Tkv;
-      const int64_t orow = (static_cast<int64_t>(t.bg) * s.Tkv + (valid ? krow : 0)) * C::D;
+      // blocks of W columns of [dV | dK] dealt round-robin over the warps of
+      // this lane quarter
+      constexpr int S = (C::D % 64 == 0 && 2 * C::D / 64 >= C::NWG) ? 8 : 4, W = 8 * S;
+      const int row0 = t.k0 + quarter * 32;
+      const int rows_valid = min(32, s.Tkv - row0);
+      const int64_t orow = static_cast<int64_t>(t.bg) * s.Tkv + (rows_valid > 0 ? row0 : 0);
 #pragma unroll 1
-      for (int chunk = wg; chunk < 2 * C::D / 16; chunk += C::NWG) {
-        const bool is_dk = chunk >= C::D / 16;
-        const int cc = (is_dk ? chunk - C::D / 16 : chunk) * 16;
-        T16* dst = reinterpret_cast<T16*>(is_dk ? dk_out : dv_out) + orow + cc;
-        store_acc_chunk16<C::BF16>(tmem + lane_base + (is_dk ? C::DK_COL : C::DV_COL) + cc, have,
-                                   is_dk ? scale : 1.f, valid, dst);
+      for (int task = wg; task < 2 * C::D / W; task += C::NWG) {
+        const bool is_dk = task * W >= C::D;
+        const int cc = is_dk ? task * W - C::D : task * W;
+        T16* dst = reinterpret_cast<T16*>(is_dk ? dk_out : dv_out) + orow * C::D + cc;
+        store_acc_block<S, C::BF16>(tmem + lane_base + (is_dk ? C::DK_COL : C::DV_COL) + cc, have,
+                                    is_dk ? scale : 1.f, dst, C::D, rows_valid);
       }
       if (have) {
         tc_fence_before();
@@ -889,13 +929,16 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         if (!ok) break;
         tc_fence_after();
       }
-      const bool valid = row < s.Tq;
-      T16* dst_row = reinterpret_cast<T16*>(dq_out) +
-                     (static_cast<int64_t>(t.bh) * s.Tq + (valid ? row : 0)) * C::D;
+      // 32-column blocks of the dQ rows dealt round-robin over the warps of
+      // this lane quarter
+      const int row0 = t.q0 + quarter * 32;
+      const int rows_valid = min(32, s.Tq - row0);
+      T16* dst_blk = reinterpret_cast<T16*>(dq_out) +
+                     (static_cast<int64_t>(t.bh) * s.Tq + (rows_valid > 0 ? row0 : 0)) * C::D;
 #pragma unroll 1
-      for (int chunk = wg; chunk < C::D / 16; chunk += C::NWG)
-        store_acc_chunk16<C::BF16>(tmem + lane_base + C::DQ_COL + 128 * buf + chunk * 16, have, scale,
-                                   valid, dst_row + chunk * 16);
+      for (int task = wg; task < C::D / 32; task += C::NWG)
+        store_acc_block<4, C::BF16>(tmem + lane_base + C::DQ_COL + 128 * buf + task * 32, have, scale,
+                                    dst_blk + task * 32, C::D, rows_valid);
       if (have) {
         tc_fence_before();
         __syncwarp();
