@@ -232,9 +232,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         for (int k = 0; k < C::BN; ++k)
           if (k0 + k >= s.Tkv || !key_visible(row, k0 + k, s.causal, s.window)) sv[k] = -INFINITY;
       }
-      float mx = -INFINITY;
+      // row max over 8 independent chains (a single chain is 128 dependent
+      // instructions long)
+      float m8[8];
 #pragma unroll
-      for (int k = 0; k < C::BN; ++k) mx = fmaxf(mx, sv[k]);
+      for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < C::BN; ++k) m8[k & 7] = fmaxf(m8[k & 7], sv[k]);
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       mx *= c;
       float alpha = 1.f;
       const bool grow = mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx > -INFINITY);
@@ -243,20 +249,25 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         m_used = mx;
       }
       const float mexp = (m_used == -INFINITY) ? 0.f : m_used;
-      float rs = 0.f;
+      // p = 2^(s c - m): arguments two at a time (f32x2), the row sum in four
+      // independent two-lane accumulators
+      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-mexp, -mexp);
+      uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int cc = 0; cc < C::BN; cc += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          const float p0 = ex2(fmaf(sv[cc + k], c, -mexp));
-          const float p1 = ex2(fmaf(sv[cc + k + 1], c, -mexp));
-          rs += p0 + p1;
+          const float2 x = f2_unpack(ffma2(f2_pack(sv[cc + k], sv[cc + k + 1]), c2, nm2));
+          const float p0 = ex2(x.x), p1 = ex2(x.y);
+          acc[(k / 2) & 3] = fadd2(acc[(k / 2) & 3], f2_pack(p0, p1));
           pk[k / 2] = pack2<C::BF16>(p0, p1);
         }
         // P overwrites the (already loaded) S columns: 2 values per column
         tmem_st16(s_addr + cc / 2, pk);
       }
+      const float2 a01 = f2_unpack(fadd2(acc[0], acc[1])), a23 = f2_unpack(fadd2(acc[2], acc[3]));
+      const float rs = (a01.x + a01.y) + (a23.x + a23.y);
       l = l * alpha + rs;
       if (it > 0 && __any_sync(0xffffffffu, grow)) {
         // O_t holds the sum of the previous tiles: wait for the last of them.
