@@ -252,6 +252,8 @@ fa_bwd_dkv_split_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
       mbar_wait(bar(B_SFULL), it & 1, wc.timeout_cycles, abort_flag, wc.status);
       tc_fence_after();
       const bool need_mask = !block_unmasked(s, i0, i0 + C::BMQ, k0, k0 + kBM);
+      int mlo, mhi;  // query columns of this tile that see this thread's key
+      visible_queries(s, krow, i0, &mlo, &mhi);
 #pragma unroll
       for (int cc = 0; cc < C::BMQ; cc += 32) {
         uint32_t sv[32], pv[32];
@@ -266,7 +268,7 @@ fa_bwd_dkv_split_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
           for (int e = 0; e < 2; ++e) {
             const int q = cc + k + e;
             float sc = __uint_as_float(sv[k + e]);
-            if (need_mask && !key_visible(i0 + q, krow, s.causal, s.window)) sc = -INFINITY;
+            if (need_mask && !(q >= mlo && q < mhi)) sc = -INFINITY;
             p[e] = ex2(fmaf(sc, c, -lse_s[q]));
             d2[e] = C::DO_DK ? p[e] * (__uint_as_float(pv[k + e]) - dv_s[q]) : 0.f;
           }
@@ -490,6 +492,8 @@ fa_bwd_dq_serial_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
       mbar_wait(bar(B_SFULL), it & 1, wc.timeout_cycles, abort_flag, wc.status);
       tc_fence_after();
       const bool need_mask = !block_unmasked(s, q0, q0 + kBM, kb, kb + C::BN);
+      int mlo, mhi;  // key columns of this tile this thread's query sees
+      visible_keys(s, row, kb, &mlo, &mhi);
 #pragma unroll
       for (int cc = 0; cc < C::BN; cc += 32) {
         uint32_t sv[32], pv[32];
@@ -502,9 +506,9 @@ fa_bwd_dq_serial_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
           float d2[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int j = kb + cc + k + e;
+            const int j = cc + k + e;
             float sc = __uint_as_float(sv[k + e]);
-            if (need_mask && (j >= s.Tkv || !key_visible(row, j, s.causal, s.window))) sc = -INFINITY;
+            if (need_mask && !(j >= mlo && j < mhi)) sc = -INFINITY;
             const float p = ex2(fmaf(sc, c, -l2));
             d2[e] = p * (__uint_as_float(pv[k + e]) - dd);
           }

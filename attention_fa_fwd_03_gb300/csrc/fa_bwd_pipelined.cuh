@@ -55,66 +55,6 @@ __host__ __device__ constexpr uint32_t chunk_operand_col(uint32_t dp_col, int kk
   return dp_col + 32 * (kk >> 1) + 8 * (kk & 1);
 }
 
-// Store a 32-row x 8S-column block of an fp32 TMEM accumulator (the warp's
-// TMEM lane quarter, columns [taddr, taddr + 8S)), scaled by `mul`, as 16-bit
-// values to rows [0, rows_valid) of `base` (row r at base + r * ld). A thread
-// holds one row, so storing it directly would make every 16-byte store of the
-// warp touch 32 rows; instead the lanes first transpose 16-byte segments
-// within groups of S lanes (log2 S butterfly exchange steps), after which each
-// store instruction writes 32 / S whole 16S-byte row segments.
-template <int S, bool BF16, class T16>
-__device__ __forceinline__ void store_acc_block(uint32_t taddr, bool have_data, float mul,
-                                                T16* base, int64_t ld, int rows_valid) {
-  static_assert(S == 4 || S == 8, "segments per row");
-  const int lane = threadIdx.x & 31;
-  uint4 a[S];  // this lane's row: S segments of 8 values
-#pragma unroll
-  for (int h = 0; h < S / 2; ++h) {
-    uint32_t v[16];
-    if (have_data) {
-      tmem_ld16(taddr + 16 * h, v);
-      tmem_ld_wait();
-    }
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float x = have_data ? __uint_as_float(v[8 * q + 2 * e]) * mul : 0.f;
-        const float y = have_data ? __uint_as_float(v[8 * q + 2 * e + 1]) * mul : 0.f;
-        w[e] = pack2<BF16>(x, y);
-      }
-      a[2 * h + q] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
-  // after the exchange, lane c of a group holds in a[j] segment c of the
-  // group's row j
-#pragma unroll
-  for (int k = S / 2; k >= 1; k >>= 1) {
-    const bool hi = (lane & k) != 0;
-#pragma unroll
-    for (int e = 0; e < S; ++e) {
-      if (e & k) continue;
-      const uint4 send = hi ? a[e] : a[e ^ k];
-      uint4 r;
-      r.x = __shfl_xor_sync(0xffffffffu, send.x, k);
-      r.y = __shfl_xor_sync(0xffffffffu, send.y, k);
-      r.z = __shfl_xor_sync(0xffffffffu, send.z, k);
-      r.w = __shfl_xor_sync(0xffffffffu, send.w, k);
-      if (hi)
-        a[e] = r;
-      else
-        a[e ^ k] = r;
-    }
-  }
-  const int g = lane / S, c = lane % S;
-#pragma unroll
-  for (int j = 0; j < S; ++j) {
-    const int r = S * g + j;
-    if (r < rows_valid) *reinterpret_cast<uint4*>(base + r * ld + 8 * c) = a[j];
-  }
-}
-
 // p[k] = 2^(s[k] * c + nl[k]) for 32 scores held as raw fp32 bits (in place).
 __device__ __forceinline__ void exp2_scores32(uint32_t (&sv)[32], uint64_t c2, const float* nl,
                                               bool per_column_nl, uint64_t nl_row) {
@@ -131,15 +71,6 @@ __device__ __forceinline__ void exp2_scores32(uint32_t (&sv)[32], uint64_t c2, c
       sv[k + e + 1] = __float_as_uint(ex2(x.y));
     }
   }
-}
-
-// After an abort, wait (bounded, whatever the abort flag says) until the last
-// `nst` loads issued into a ring of `nst` slots have landed, so that no copy is
-// still in flight into this CTA's shared memory when it exits.
-__device__ __forceinline__ void drain_ring(uint32_t full_bar0, int nst, int issued,
-                                           uint64_t tmo, uint32_t* status) {
-  for (int i = issued > nst ? issued - nst : 0; i < issued; ++i)
-    mbar_wait(full_bar0 + 8u * static_cast<uint32_t>(i % nst), (i / nst) & 1, tmo, nullptr, status);
 }
 
 // ---------------------------------------------------------------- dK / dV
@@ -491,10 +422,11 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const float* nl_s = stats + slot * 2 * C::BMQ + wg * C::CW;  // -LSE * log2(e)
         const float* nd_s = nl_s + C::BMQ;                           // -D
         if (!block_unmasked(s, i0, i0 + C::BMQ, t.k0, t.k0 + kBM)) {
+          int lo, hi;
+          visible_queries(s, krow, i0 + wg * C::CW, &lo, &hi);
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            if (!key_visible(i0 + wg * C::CW + q, krow, s.causal, s.window))
-              sv[q] = __float_as_uint(-INFINITY);
+            sv[q] = (q >= lo && q < hi) ? sv[q] : __float_as_uint(-INFINITY);
         }
         exp2_scores32(sv, c2, nl_s, true, 0);  // sv now holds P (fp32)
         // dS^T = P^T o (dP^T - D) once dP^T(it) is in TMEM
@@ -879,12 +811,11 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_SFREE));  // the next S may overwrite them
         if (!block_unmasked(s, t.q0, t.q0 + kBM, kb, kb + C::CW)) {
+          int lo, hi;
+          visible_keys(s, row, kb, &lo, &hi);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int j = kb + q;
-            if (j >= s.Tkv || !key_visible(row, j, s.causal, s.window))
-              sv[q] = __float_as_uint(-INFINITY);
-          }
+          for (int q = 0; q < 32; ++q)
+            sv[q] = (q >= lo && q < hi) ? sv[q] : __float_as_uint(-INFINITY);
         }
         exp2_scores32(sv, c2, nullptr, false, nl2x2);  // sv now holds P (fp32)
         ok = mbar_wait(bar(C::B_DPFULL), gi & 1, tmo, abort_flag, wc.status);

@@ -100,6 +100,28 @@ __host__ __device__ __forceinline__ bool key_visible(int i, int j, int causal, i
   return true;
 }
 
+// The same mask as intervals, for masking a tile with one compare-and-select
+// per element (evaluating key_visible per element of a 128-wide unrolled row
+// costs thousands of cycles per tile).
+//
+// Keys visible to query i, relative to key k0: [lo, hi) (may be empty or reach
+// past either end of a tile); keys at or beyond Tkv are excluded.
+__host__ __device__ __forceinline__ void visible_keys(const AttnShape& s, int i, int k0, int* lo,
+                                                      int* hi) {
+  const int h = s.causal ? min(i + 1, s.Tkv) : s.Tkv;
+  const int l = s.window > 0 ? i - s.window + 1 : -(1 << 30);
+  *lo = max(l - k0, -(1 << 30));
+  *hi = h - k0;
+}
+
+// Queries that see key j, relative to query i0: [lo, hi) (queries at or beyond
+// Tq are not excluded here).
+__host__ __device__ __forceinline__ void visible_queries(const AttnShape& s, int j, int i0, int* lo,
+                                                         int* hi) {
+  *lo = s.causal ? j - i0 : -(1 << 30);
+  *hi = s.window > 0 ? j + s.window - i0 : (1 << 30);
+}
+
 // Keys that any query in [q_lo, q_hi) can see: [first, last) (may be empty).
 __host__ __device__ __forceinline__ void key_range(const AttnShape& s, int q_lo, int q_hi,
                                                    int* first, int* last) {
@@ -128,6 +150,75 @@ __host__ __device__ __forceinline__ bool block_unmasked(const AttnShape& s, int 
   if (s.causal && k_hi - 1 > q_lo) return false;
   if (s.window > 0 && (q_hi - 1) - k_lo >= s.window) return false;
   return true;
+}
+
+// After an abort, wait (bounded, whatever the abort flag says) until the last
+// `nst` loads issued into a ring of `nst` slots have landed, so that no copy is
+// still in flight into this CTA's shared memory when it exits.
+__device__ __forceinline__ void drain_ring(uint32_t full_bar0, int nst, int issued,
+                                           uint64_t tmo, uint32_t* status) {
+  for (int i = issued > nst ? issued - nst : 0; i < issued; ++i)
+    mbar_wait(full_bar0 + 8u * static_cast<uint32_t>(i % nst), (i / nst) & 1, tmo, nullptr, status);
+}
+
+// Store a 32-row x 8S-column block of an fp32 TMEM accumulator (the warp's
+// TMEM lane quarter, columns [taddr, taddr + 8S)), scaled by `mul`, as 16-bit
+// values to rows [0, rows_valid) of `base` (row r at base + r * ld). A thread
+// holds one row, so storing it directly would make every 16-byte store of the
+// warp touch 32 rows; instead the lanes first transpose 16-byte segments
+// within groups of S lanes (log2 S butterfly exchange steps), after which each
+// store instruction writes 32 / S whole 16S-byte row segments.
+template <int S, bool BF16, class T16>
+__device__ __forceinline__ void store_acc_block(uint32_t taddr, bool have_data, float mul,
+                                                T16* base, int64_t ld, int rows_valid) {
+  static_assert(S == 4 || S == 8, "segments per row");
+  const int lane = threadIdx.x & 31;
+  uint4 a[S];  // this lane's row: S segments of 8 values
+#pragma unroll
+  for (int h = 0; h < S / 2; ++h) {
+    uint32_t v[16];
+    if (have_data) {
+      tmem_ld16(taddr + 16 * h, v);
+      tmem_ld_wait();
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = have_data ? __uint_as_float(v[8 * q + 2 * e]) * mul : 0.f;
+        const float y = have_data ? __uint_as_float(v[8 * q + 2 * e + 1]) * mul : 0.f;
+        w[e] = pack2<BF16>(x, y);
+      }
+      a[2 * h + q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  // after the exchange, lane c of a group holds in a[j] segment c of the
+  // group's row j
+#pragma unroll
+  for (int k = S / 2; k >= 1; k >>= 1) {
+    const bool hi = (lane & k) != 0;
+#pragma unroll
+    for (int e = 0; e < S; ++e) {
+      if (e & k) continue;
+      const uint4 send = hi ? a[e] : a[e ^ k];
+      uint4 r;
+      r.x = __shfl_xor_sync(0xffffffffu, send.x, k);
+      r.y = __shfl_xor_sync(0xffffffffu, send.y, k);
+      r.z = __shfl_xor_sync(0xffffffffu, send.z, k);
+      r.w = __shfl_xor_sync(0xffffffffu, send.w, k);
+      if (hi)
+        a[e] = r;
+      else
+        a[e ^ k] = r;
+    }
+  }
+  const int g = lane / S, c = lane % S;
+#pragma unroll
+  for (int j = 0; j < S; ++j) {
+    const int r = S * g + j;
+    if (r < rows_valid) *reinterpret_cast<uint4*>(base + r * ld + 8 * c) = a[j];
+  }
 }
 
 }  // namespace fa

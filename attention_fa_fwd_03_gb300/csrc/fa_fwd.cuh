@@ -21,6 +21,12 @@
 //                finally normalises O_t and writes O and LSE.
 // With NQ = 2 the two softmax warpgroups ping-pong: while one computes its
 // softmax the tensor core works on the other tile's MMAs.
+// Persistent: a CTA that finishes its block takes over the next
+// not-yet-started CTA's block through cluster launch control (ItemQueue), so
+// one CTA per SM walks a balanced stream of blocks in launch order. The K/V
+// ring runs on across blocks, the next block's first scores are computed
+// while the softmax warpgroups store the previous block, and Q is reloaded
+// once the block's last score MMA has read it.
 #pragma once
 
 #include "fa_common.cuh"
@@ -32,6 +38,27 @@ namespace fa {
 // so unnormalised P stays below 2^8. The final O = o / l and LSE = m + log2 l
 // use the same max, so the result is exact.
 constexpr float kRescaleThreshold = 8.0f;
+
+// One forward work item: a (batch, head) and a block of NQ * 128 query rows;
+// its tiles are the key tiles the block sees.
+struct FwdItem {
+  int bh, b, g, q0, j_lo, n_iter;
+};
+
+__device__ __forceinline__ FwdItem fwd_item(int linear, const TileOrder& o, const AttnShape& s,
+                                            int rows, int bn) {
+  FwdItem t;
+  int qblk;
+  decode_tile(linear, o, &t.bh, &qblk);
+  t.b = t.bh / s.Hq;
+  t.g = (t.bh - t.b * s.Hq) / (s.Hq / s.Hkv);
+  t.q0 = qblk * rows;
+  int k_first, k_last;
+  key_range(s, t.q0, min(s.Tq, t.q0 + rows), &k_first, &k_last);
+  t.j_lo = k_first / bn;
+  t.n_iter = max(0, (k_last + bn - 1) / bn - t.j_lo);
+  return t;
+}
 
 template <int D_, int NQ_, int BN_, int STAGES_, bool BF16_>
 struct FwdCfg {
@@ -50,12 +77,24 @@ struct FwdCfg {
   static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
   static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE;
-  // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[NQ], p_full[NQ],
-  // o_ready[NQ], drain
-  static constexpr int NBAR = 1 + 3 * STAGES + 3 * NQ + 1;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  // barriers: q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[NQ],
+  // p_full[NQ], o_ready[NQ], drain, item responses full[kClcSlots] / empty[kClcSlots]
+  static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = B_KFULL + STAGES,
+                       B_KVEMPTY = B_VFULL + STAGES, B_SFULL = B_KVEMPTY + STAGES,
+                       B_PFULL = B_SFULL + NQ, B_OREADY = B_PFULL + NQ, B_DRAIN = B_OREADY + NQ,
+                       B_CLCFULL = B_DRAIN + 1, B_CLCEMPTY = B_CLCFULL + kClcSlots,
+                       NBAR = B_CLCEMPTY + kClcSlots;
+  static constexpr int OFF_CLC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;
+  static constexpr int OFF_MISC = OFF_CLC + 16 * kClcSlots;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 128 + NQ * 128;
+  static constexpr int ITEM_WARPS = 2 + 4 * NQ;  // warps that walk the items: 0, 1, softmax
+  // Registers per thread after the split (0: no split): the producer / MMA
+  // warpgroup hands registers to the softmax warpgroups, whose 128-score rows
+  // would otherwise spill. The launch must hold THREADS x launch registers >=
+  // REG_NEEDED (checked on the host against the compiled kernel).
+  static constexpr int REG_CTRL = NQ == 2 ? 80 : 0, REG_SOFT = NQ == 2 ? 200 : 0;
+  static constexpr int REG_NEEDED = 128 * REG_CTRL + 128 * NQ * REG_SOFT;
   static constexpr int S_COL(int t) { return t * 128; }
   static constexpr int O_COL(int t) { return 256 + t * 128; }
   static constexpr uint32_t TMEM_COLS = 512;
@@ -77,28 +116,20 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   auto bar = [&](int i) { return smem_u32(bars + i); };
-  const int B_QFULL = 0, B_KFULL = 1, B_VFULL = 1 + C::STAGES, B_KVEMPTY = 1 + 2 * C::STAGES,
-            B_SFULL = 1 + 3 * C::STAGES, B_PFULL = B_SFULL + C::NQ, B_OREADY = B_PFULL + C::NQ,
-            B_DRAIN = B_OREADY + C::NQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-
-  // ---- work item: a (batch, head) and a block of NQ*128 query rows
-  int bh, qblk;
-  decode_tile(blockIdx.x, order, &bh, &qblk);
-  const int b = bh / s.Hq, h = bh % s.Hq;
-  const int g = h / (s.Hq / s.Hkv);
-  const int q0 = qblk * (C::NQ * kBM);
-  int k_first, k_last;
-  key_range(s, q0, min(s.Tq, q0 + C::NQ * kBM), &k_first, &k_last);
-  const int j_lo = k_first / C::BN;
-  const int j_hi = (k_last + C::BN - 1) / C::BN;
-  const int n_iter = max(0, j_hi - j_lo);
+  const uint64_t tmo = wc.timeout_cycles;
+  const ItemQueue iq{sbase + C::OFF_CLC, bar(C::B_CLCFULL), bar(C::B_CLCEMPTY)};
+  constexpr int ROWS = C::NQ * kBM;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < C::NBAR; ++i)
-      mbar_init(bar(i), (i >= B_PFULL && i < B_PFULL + C::NQ) ? 128u : 1u);
+    for (int i = 0; i < C::NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i >= C::B_PFULL && i < C::B_PFULL + C::NQ) cnt = 128;  // every softmax thread
+      if (i >= C::B_CLCEMPTY && i < C::B_CLCEMPTY + kClcSlots) cnt = C::ITEM_WARPS;
+      mbar_init(bar(i), cnt);
+    }
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -110,217 +141,272 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < 4) {
+  if constexpr (C::REG_CTRL > 0) regs_release<C::REG_CTRL>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (n_iter > 0) {
-      // the whole warp runs the loop (a lone active lane whose siblings wait at
-      // the final barrier issues far slower); one elected lane issues
-      const bool leader = elect_one_sync();
-      if (leader) tma_prefetch_desc(&map_q);
-      if (leader) tma_prefetch_desc(&map_k);
-      if (leader) tma_prefetch_desc(&map_v);
-      if (leader) mbar_arrive_expect_tx(bar(B_QFULL), C::NQ * C::Q_TILE);
-      for (int t = 0; t < C::NQ; ++t)
-        for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(sbase + C::OFF_Q + t * C::Q_TILE + r * C::Q_REGION, &map_q, bar(B_QFULL),
-                      r * 64, q0 + t * kBM, bh);
-      const int zkv = b * s.Hkv + g;
-      for (int it = 0; it < n_iter; ++it) {
-        const int st = it % C::STAGES;
-        if (it >= C::STAGES)
-          mbar_wait(bar(B_KVEMPTY + st), ((it / C::STAGES) - 1) & 1, wc.timeout_cycles, abort_flag,
-                    wc.status);
-        const int krow = (j_lo + it) * C::BN;
-        if (leader) mbar_arrive_expect_tx(bar(B_KFULL + st), C::KV_TILE);
-        for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(sbase + C::OFF_K + st * C::KV_TILE + r * C::KV_REGION, &map_k,
-                      bar(B_KFULL + st), r * 64, krow, zkv);
-        if (leader) mbar_arrive_expect_tx(bar(B_VFULL + st), C::KV_TILE);
-        for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(sbase + C::OFF_V + st * C::KV_TILE + r * C::KV_REGION, &map_v,
-                      bar(B_VFULL + st), r * 64, krow, zkv);
+    // Q of each block once its previous contents were last read, then the
+    // block's K_j / V_j into the ring (and the item requests). The whole warp
+    // runs the loop (a lone active lane whose siblings wait at the final
+    // barrier issues far slower); one elected lane issues.
+    const bool leader = elect_one_sync();
+    if (leader) tma_prefetch_desc(&map_q);
+    if (leader) tma_prefetch_desc(&map_k);
+    if (leader) tma_prefetch_desc(&map_v);
+    int gk = 0, ln = 0, asked = 0;  // ring tiles issued, blocks with work, requests
+    bool ok = true;
+    for (int k = 0, item = blockIdx.x; ok; ++k) {
+      ok = clc_request(iq, k, leader, tmo, abort_flag, wc.status);
+      if (!ok) break;
+      ++asked;
+      const FwdItem t = fwd_item(item, order, s, ROWS, C::BN);
+      if (t.n_iter > 0) {
+        if (ln > 0) ok = mbar_wait(bar(C::B_QEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL), C::NQ * C::Q_TILE);
+        for (int tq = 0; tq < C::NQ; ++tq)
+          for (int r = 0; r < C::KREG; ++r)
+            if (leader)
+              tma_load_3d(sbase + C::OFF_Q + tq * C::Q_TILE + r * C::Q_REGION, &map_q, bar(C::B_QFULL),
+                          r * 64, t.q0 + tq * kBM, t.bh);
+        ++ln;
+        const int zkv = t.b * s.Hkv + t.g;
+        for (int it = 0; it < t.n_iter; ++it, ++gk) {
+          const int st = gk % C::STAGES;
+          if (gk >= C::STAGES)
+            ok = mbar_wait(bar(C::B_KVEMPTY + st), ((gk / C::STAGES) - 1) & 1, tmo, abort_flag, wc.status);
+          if (!ok) break;
+          const int krow = (t.j_lo + it) * C::BN;
+          if (leader) mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::KV_TILE);
+          for (int r = 0; r < C::KREG; ++r)
+            if (leader)
+              tma_load_3d(sbase + C::OFF_K + st * C::KV_TILE + r * C::KV_REGION, &map_k,
+                          bar(C::B_KFULL + st), r * 64, krow, zkv);
+          if (leader) mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::KV_TILE);
+          for (int r = 0; r < C::KREG; ++r)
+            if (leader)
+              tma_load_3d(sbase + C::OFF_V + st * C::KV_TILE + r * C::KV_REGION, &map_v,
+                          bar(C::B_VFULL + st), r * 64, krow, zkv);
+        }
+        if (!ok) break;
       }
+      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
+    }
+    if (*abort_flag) {
+      drain_ring(bar(C::B_QFULL), 1, ln, tmo, wc.status);
+      drain_ring(bar(C::B_KFULL), C::STAGES, gk, tmo, wc.status);
+      drain_ring(bar(C::B_VFULL), C::STAGES, gk, tmo, wc.status);
+      drain_ring(iq.full, kClcSlots, asked, tmo, wc.status);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
-    if (n_iter > 0) {
-      // the whole warp runs the loop (a lone active lane whose siblings wait at
-      // the final barrier issues far slower); one elected lane issues
-      const bool leader = elect_one_sync();
-      constexpr uint32_t idesc_s = make_idesc_f16(kBM, C::BN, C::BF16 ? 1 : 0, 0, 0);
-      constexpr uint32_t idesc_o = make_idesc_f16(kBM, C::D, C::BF16 ? 1 : 0, 0, 1);
-      auto issue_s = [&](int t, int st) {
-        const uint32_t qa = sbase + C::OFF_Q + t * C::Q_TILE;
-        const uint32_t ka = sbase + C::OFF_K + st * C::KV_TILE;
+    // the whole warp runs the loop; one elected lane issues
+    const bool leader = elect_one_sync();
+    constexpr uint32_t idesc_s = make_idesc_f16(kBM, C::BN, C::BF16 ? 1 : 0, 0, 0);
+    constexpr uint32_t idesc_o = make_idesc_f16(kBM, C::D, C::BF16 ? 1 : 0, 0, 1);
+    auto issue_s = [&](int tq, int st) {
+      const uint32_t qa = sbase + C::OFF_Q + tq * C::Q_TILE;
+      const uint32_t ka = sbase + C::OFF_K + st * C::KV_TILE;
 #pragma unroll
-        for (int kk = 0; kk < C::D / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;  // 16 elements = 32 bytes along K
-          const uint64_t ad = make_sdesc(qa + (kk >> 2) * C::Q_REGION + off, 16, 1024, 2);
-          const uint64_t bd = make_sdesc(ka + (kk >> 2) * C::KV_REGION + off, 16, 1024, 2);
-          if (leader) mma_ss(tmem + C::S_COL(t), ad, bd, idesc_s, kk > 0);
-        }
-      };
-      auto issue_pv = [&](int t, int st, bool acc) {
-        const uint32_t va = sbase + C::OFF_V + st * C::KV_TILE;
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          const uint64_t bd = make_sdesc(va + kk * 16 * 128, C::KV_REGION, 1024, 2);
-          if (leader) mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, bd, idesc_o,
-                 (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-      mbar_wait(bar(B_QFULL), 0, wc.timeout_cycles, abort_flag, wc.status);
-      mbar_wait(bar(B_KFULL + 0), 0, wc.timeout_cycles, abort_flag, wc.status);
-      tc_fence_after();
-      for (int t = 0; t < C::NQ; ++t) {
-        if (leader) issue_s(t, 0);
-        if (leader) mma_commit(bar(B_SFULL + t));
+      for (int kk = 0; kk < C::D / 16; ++kk) {
+        const uint32_t off = (kk & 3) * 32;  // 16 elements = 32 bytes along K
+        const uint64_t ad = make_sdesc(qa + (kk >> 2) * C::Q_REGION + off, 16, 1024, 2);
+        const uint64_t bd = make_sdesc(ka + (kk >> 2) * C::KV_REGION + off, 16, 1024, 2);
+        if (leader) mma_ss(tmem + C::S_COL(tq), ad, bd, idesc_s, kk > 0);
       }
-      for (int it = 0; it < n_iter; ++it) {
-        const int st = it % C::STAGES;
-        const int nst = (it + 1) % C::STAGES;
-        mbar_wait(bar(B_VFULL + st), (it / C::STAGES) & 1, wc.timeout_cycles, abort_flag, wc.status);
-        for (int t = 0; t < C::NQ; ++t) {
-          mbar_wait(bar(B_PFULL + t), it & 1, wc.timeout_cycles, abort_flag, wc.status);
-          tc_fence_after();
-          if (leader) issue_pv(t, st, it > 0);
-          if (leader) mma_commit(bar(B_OREADY + t));
-          if (it + 1 < n_iter) {
-            if (t == 0) {
-              mbar_wait(bar(B_KFULL + nst), ((it + 1) / C::STAGES) & 1, wc.timeout_cycles, abort_flag,
-                        wc.status);
-              tc_fence_after();
+    };
+    auto issue_pv = [&](int tq, int st, bool acc) {
+      const uint32_t va = sbase + C::OFF_V + st * C::KV_TILE;
+#pragma unroll
+      for (int kk = 0; kk < C::BN / 16; ++kk) {
+        const uint64_t bd = make_sdesc(va + kk * 16 * 128, C::KV_REGION, 1024, 2);
+        if (leader)
+          mma_ts(tmem + C::O_COL(tq), tmem + C::S_COL(tq) + kk * 8, bd, idesc_o, (acc || kk > 0) ? 1u : 0u);
+      }
+    };
+    auto wait = [&](int b, int parity) {
+      return mbar_wait(bar(b), parity & 1, tmo, abort_flag, wc.status);
+    };
+    int gk = 0, ln = 0;
+    bool ok = true;
+    for (int k = 0, item = blockIdx.x; ok; ++k) {
+      const FwdItem t = fwd_item(item, order, s, ROWS, C::BN);
+      const int n = t.n_iter;
+      if (n > 0) {
+        // scores of the block's first key tile (over the P columns of the
+        // previous block, whose PV MMAs precede them in issue order)
+        ok = wait(C::B_QFULL, ln) && wait(C::B_KFULL + gk % C::STAGES, gk / C::STAGES);
+        if (!ok) break;
+        tc_fence_after();
+        for (int tq = 0; tq < C::NQ; ++tq) {
+          if (leader) issue_s(tq, gk % C::STAGES);
+          if (leader) mma_commit(bar(C::B_SFULL + tq));
+        }
+        if (n == 1 && leader) mma_commit(bar(C::B_QEMPTY));  // Q read for the last time
+        for (int it = 0; it < n; ++it) {
+          const int gi = gk + it;
+          const int st = gi % C::STAGES, nst = (gi + 1) % C::STAGES;
+          ok = wait(C::B_VFULL + st, gi / C::STAGES);
+          if (!ok) break;
+          for (int tq = 0; tq < C::NQ; ++tq) {
+            // P_t in TMEM; for the block's first tile this also means the
+            // softmax warpgroup has stored the previous block's O_t
+            ok = wait(C::B_PFULL + tq, gi);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) issue_pv(tq, st, it > 0);
+            if (leader) mma_commit(bar(C::B_OREADY + tq));
+            if (it + 1 < n) {
+              if (tq == 0) {
+                ok = wait(C::B_KFULL + nst, (gi + 1) / C::STAGES);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              if (leader) issue_s(tq, nst);
+              if (leader) mma_commit(bar(C::B_SFULL + tq));
             }
-            if (leader) issue_s(t, nst);
-            if (leader) mma_commit(bar(B_SFULL + t));
           }
+          if (!ok) break;
+          if (it + 2 == n && leader) mma_commit(bar(C::B_QEMPTY));
+          if (leader) mma_commit(bar(C::B_KVEMPTY + st));
         }
-        if (leader) mma_commit(bar(B_KVEMPTY + st));
+        if (!ok) break;
+        gk += n;
+        ++ln;
       }
-      // make sure nothing is in flight before TMEM is released
-      if (leader) mma_commit(bar(B_DRAIN));
-      mbar_wait(bar(B_DRAIN), 0, wc.timeout_cycles, nullptr, wc.status);
+      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
     }
-  } else if (warp >= 4) {
+    // make sure nothing is in flight before TMEM is released
+    if (leader) mma_commit(bar(C::B_DRAIN));
+    mbar_wait(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
+  }
+  } else {
+    if constexpr (C::REG_SOFT > 0) regs_claim<C::REG_SOFT>();
     // ------------------------------------------------------------- softmax
-    const int t = (warp - 4) >> 2;              // query tile of this warpgroup
+    const int tq = (warp - 4) >> 2;             // query tile of this warpgroup
     const int quarter = warp & 3;               // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;          // row within the tile
-    const int row = q0 + t * kBM + r;
-    const int tq_lo = q0 + t * kBM;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_addr = tmem + lane_base + C::S_COL(t);
-    const uint32_t o_addr = tmem + lane_base + C::O_COL(t);
+    const uint32_t s_addr = tmem + lane_base + C::S_COL(tq);
+    const uint32_t o_addr = tmem + lane_base + C::O_COL(tq);
     const float c = s.scale_log2;
-
-    float m_used = -INFINITY;  // max used for the exponentials (log2 domain)
-    float l = 0.f;
-    for (int it = 0; it < n_iter; ++it) {
-      const int k0 = (j_lo + it) * C::BN;
-      mbar_wait(bar(B_SFULL + t), it & 1, wc.timeout_cycles, abort_flag, wc.status);
-      tc_fence_after();
-      uint32_t sr[C::BN];
-#pragma unroll
-      for (int cc = 0; cc < C::BN; cc += 32)
-        tmem_ld32(s_addr + cc, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc]));
-      tmem_ld_wait();
-      float sv[C::BN];
-#pragma unroll
-      for (int k = 0; k < C::BN; ++k) sv[k] = __uint_as_float(sr[k]);
-      if (!block_unmasked(s, tq_lo, tq_lo + kBM, k0, k0 + C::BN)) {
-#pragma unroll
-        for (int k = 0; k < C::BN; ++k)
-          if (k0 + k >= s.Tkv || !key_visible(row, k0 + k, s.causal, s.window)) sv[k] = -INFINITY;
-      }
-      // row max over 8 independent chains (a single chain is 128 dependent
-      // instructions long)
-      float m8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < C::BN; ++k) m8[k & 7] = fmaxf(m8[k & 7], sv[k]);
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      mx *= c;
-      float alpha = 1.f;
-      const bool grow = mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx > -INFINITY);
-      if (grow) {
-        alpha = ex2(m_used - mx);  // 0 when m_used = -inf
-        m_used = mx;
-      }
-      const float mexp = (m_used == -INFINITY) ? 0.f : m_used;
-      // p = 2^(s c - m): arguments two at a time (f32x2), the row sum in four
-      // independent two-lane accumulators
-      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-mexp, -mexp);
-      uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int cc = 0; cc < C::BN; cc += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float2 x = f2_unpack(ffma2(f2_pack(sv[cc + k], sv[cc + k + 1]), c2, nm2));
-          const float p0 = ex2(x.x), p1 = ex2(x.y);
-          acc[(k / 2) & 3] = fadd2(acc[(k / 2) & 3], f2_pack(p0, p1));
-          pk[k / 2] = pack2<C::BF16>(p0, p1);
-        }
-        // P overwrites the (already loaded) S columns: 2 values per column
-        tmem_st16(s_addr + cc / 2, pk);
-      }
-      const float2 a01 = f2_unpack(fadd2(acc[0], acc[1])), a23 = f2_unpack(fadd2(acc[2], acc[3]));
-      const float rs = (a01.x + a01.y) + (a23.x + a23.y);
-      l = l * alpha + rs;
-      if (it > 0 && __any_sync(0xffffffffu, grow)) {
-        // O_t holds the sum of the previous tiles: wait for the last of them.
-        mbar_wait(bar(B_OREADY + t), (it - 1) & 1, wc.timeout_cycles, abort_flag, wc.status);
-        tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < C::D; cc += 32) {
-          uint32_t ov[32];
-          tmem_ld32(o_addr + cc, ov);
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
-          tmem_st32(o_addr + cc, ov);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(B_PFULL + t));
-    }
-
-    // ------------------------------------------------------------ epilogue
-    if (n_iter > 0) {
-      mbar_wait(bar(B_OREADY + t), (n_iter - 1) & 1, wc.timeout_cycles, abort_flag, wc.status);
-      tc_fence_after();
-    }
-    const bool valid = row < s.Tq;
-    const float inv_l = l > 0.f ? 1.f / l : 0.f;
     using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
-    T16* orow = reinterpret_cast<T16*>(o_out) +
-                ((static_cast<int64_t>(bh) * s.Tq + (valid ? row : 0)) * C::D);
-#pragma unroll 1
-    for (int cc = 0; cc < C::D; cc += 32) {
-      uint32_t ov[32];
-      if (n_iter > 0) {
-        tmem_ld32(o_addr + cc, ov);
+    int gk = 0;
+    bool ok = true;
+    for (int k = 0, item = blockIdx.x; ok; ++k) {
+      const FwdItem t = fwd_item(item, order, s, ROWS, C::BN);
+      const int tq_lo = t.q0 + tq * kBM;
+      const int row = tq_lo + r;
+      float m_used = -INFINITY;  // max used for the exponentials (log2 domain)
+      float l = 0.f;
+      for (int it = 0; it < t.n_iter; ++it) {
+        const int gi = gk + it;
+        const int k0 = (t.j_lo + it) * C::BN;
+        ok = mbar_wait(bar(C::B_SFULL + tq), gi & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        tc_fence_after();
+        // one TMEM round trip for the whole row (a load issued while the tensor
+        // core streams through TMEM takes long; a second pass would double it)
+        uint32_t sv[C::BN];
+#pragma unroll
+        for (int cc = 0; cc < C::BN; cc += 32)
+          tmem_ld32(s_addr + cc, *reinterpret_cast<uint32_t(*)[32]>(&sv[cc]));
         tmem_ld_wait();
-      }
-      uint32_t w[16];
+        if (!block_unmasked(s, tq_lo, tq_lo + kBM, k0, k0 + C::BN)) {
+          int lo, hi;
+          visible_keys(s, row, k0, &lo, &hi);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float a = n_iter > 0 ? __uint_as_float(ov[2 * k]) * inv_l : 0.f;
-        const float bb = n_iter > 0 ? __uint_as_float(ov[2 * k + 1]) * inv_l : 0.f;
-        w[k] = pack2<C::BF16>(a, bb);
-      }
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+          for (int kx = 0; kx < C::BN; ++kx)
+            sv[kx] = (kx >= lo && kx < hi) ? sv[kx] : __float_as_uint(-INFINITY);
+        }
+        // row max over 8 independent chains (a single chain is 128 dependent
+        // instructions long)
+        float m8[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+        for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
+#pragma unroll
+        for (int kx = 0; kx < C::BN; ++kx) m8[kx & 7] = fmaxf(m8[kx & 7], __uint_as_float(sv[kx]));
+        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        mx *= c;
+        float alpha = 1.f;
+        const bool grow = mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx > -INFINITY);
+        if (grow) {
+          alpha = ex2(m_used - mx);  // 0 when m_used = -inf
+          m_used = mx;
+        }
+        const float mexp = (m_used == -INFINITY) ? 0.f : m_used;
+        // p = 2^(s c - m): arguments two at a time (f32x2), the row sum in four
+        // independent two-lane accumulators
+        const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-mexp, -mexp);
+        uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int cc = 0; cc < C::BN; cc += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int kx = 0; kx < 32; kx += 2) {
+            const float2 x = f2_unpack(ffma2(
+                f2_pack(__uint_as_float(sv[cc + kx]), __uint_as_float(sv[cc + kx + 1])), c2, nm2));
+            const float p0 = ex2(x.x), p1 = ex2(x.y);
+            acc[(kx / 2) & 3] = fadd2(acc[(kx / 2) & 3], f2_pack(p0, p1));
+            pk[kx / 2] = pack2<C::BF16>(p0, p1);
+          }
+          // P overwrites the (already loaded) S columns: 2 values per column
+          tmem_st16(s_addr + cc / 2, pk);
+        }
+        const float2 a01 = f2_unpack(fadd2(acc[0], acc[1])), a23 = f2_unpack(fadd2(acc[2], acc[3]));
+        const float rs = (a01.x + a01.y) + (a23.x + a23.y);
+        l = l * alpha + rs;
+        if (it > 0 && __any_sync(0xffffffffu, grow)) {
+          // O_t holds the sum of the previous tiles: wait for the last of them.
+          ok = mbar_wait(bar(C::B_OREADY + tq), (gi - 1) & 1, tmo, abort_flag, wc.status);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < C::D; cc += 32) {
+            uint32_t ov[32];
+            tmem_ld32(o_addr + cc, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int kx = 0; kx < 32; ++kx) ov[kx] = __float_as_uint(__uint_as_float(ov[kx]) * alpha);
+            tmem_st32(o_addr + cc, ov);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PFULL + tq));
       }
+      if (!ok) break;
+
+      // ------------------------------------------------------- block epilogue
+      // O = o / l in blocks of 8S columns per warp (rows exchanged across lanes
+      // for whole-segment stores), LSE = (m + log2 l) ln 2 per row. The next
+      // block's first PV (which overwrites O_t) waits for this warpgroup's next
+      // P, which comes after these reads.
+      const bool have = t.n_iter > 0;
+      if (have) {
+        ok = mbar_wait(bar(C::B_OREADY + tq), (gk + t.n_iter - 1) & 1, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      constexpr int S = (C::D % 64 == 0) ? 8 : 4, W = 8 * S;
+      const int row0 = tq_lo + quarter * 32;
+      const int rows_valid = min(32, s.Tq - row0);
+      T16* blk = reinterpret_cast<T16*>(o_out) +
+                 (static_cast<int64_t>(t.bh) * s.Tq + (rows_valid > 0 ? row0 : 0)) * C::D;
+#pragma unroll 1
+      for (int cc = 0; cc < C::D; cc += W)
+        store_acc_block<S, C::BF16>(o_addr + cc, have, inv_l, blk + cc, C::D, rows_valid);
+      if (row < s.Tq)
+        lse_out[static_cast<int64_t>(t.bh) * s.Tq + row] =
+            l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      if (have) {
+        tc_fence_before();
+        gk += t.n_iter;
+      }
+      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
     }
-    if (valid)
-      lse_out[static_cast<int64_t>(bh) * s.Tq + row] =
-          l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
   }
 
   tc_fence_before();

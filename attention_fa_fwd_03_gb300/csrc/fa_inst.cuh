@@ -10,6 +10,16 @@
 
 namespace fa {
 
+// A kernel that moves registers between its warpgroups (setmaxnreg) may only
+// be launched when its launch-time registers cover the new counts; otherwise
+// an increase would wait forever. Checked once per kernel.
+inline bool register_split_fits(const void* kern, int threads, int needed) {
+  if (needed <= 0) return true;
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return false;
+  return static_cast<int64_t>(attr.numRegs) * threads >= needed;
+}
+
 // Units per chunk so that the operands the units' tiles share stay in L2:
 // about 32 MiB of them at a time (the L2 holds 126 MiB, and the streamed
 // per-tile operands and outputs pass through it too), rounded to a multiple
@@ -61,6 +71,8 @@ cudaError_t run_fwd(const FwdLaunch& a) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if (!register_split_fits(reinterpret_cast<const void*>(kern), C::THREADS, C::REG_NEEDED))
+    return cudaErrorInvalidConfiguration;
   const TileOrder order = query_block_order(a.s, C::NQ * kBM, C::D);
   kern<<<order.units * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, a.o, a.lse,
                                                                            a.s, order, a.wc);

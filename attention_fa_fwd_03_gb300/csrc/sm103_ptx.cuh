@@ -333,6 +333,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// ------------------------------------------------------- register split
+// Move registers between the warpgroups of a CTA. Every warp of a warpgroup
+// executes the same call, and the code a warpgroup runs afterwards sits in the
+// branch that made the call (the compiler allocates that branch against the
+// new count). An increase waits until decreases elsewhere have returned enough
+// registers, so the new counts must fit the launch's total (threads x
+// registers per thread at launch); the host checks that before launching.
+template <uint32_t N>
+__device__ __forceinline__ void regs_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_claim() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
 // ------------------------------------------------------------------ numerics
 // 2^x with the hardware approximation (ex2.approx, flushes subnormals).
 __device__ __forceinline__ float ex2(float x) {
