@@ -129,6 +129,12 @@ struct DkvCfg {
   static constexpr int OFF_MISC = OFF_CLC + 16 * kClcSlots;
   static constexpr int SMEM_BYTES = OFF_MISC + 16;  // base must be 1024-aligned (checked)
   static constexpr int THREADS = 128 + 128 * NWG;
+  // Registers per thread after the warpgroup split (0: no split); the launch
+  // must hold THREADS x launch registers >= REG_NEEDED (checked on the host).
+  // Off here: at 64 per thread the producer / MMA / staging code spills, and
+  // that costs more than the softmax spills it would remove (measured).
+  static constexpr int REG_CTRL = 0, REG_SOFT = 0;
+  static constexpr int REG_NEEDED = REG_SOFT > 0 ? 128 * REG_CTRL + 128 * NWG * REG_SOFT : 0;
   static constexpr int S_COL = 0;     // S^T block, 128 fp32 columns
   static constexpr int DP_COL = 128;  // dP^T block, 128 fp32 columns
   static constexpr int DV_COL = 256;
@@ -187,6 +193,9 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < 4) {
+  // producer / MMA / staging warpgroup: registers handed to the softmax
+  if constexpr (C::REG_SOFT > 0) regs_release<C::REG_CTRL>();
   if (warp == 0 || warp == 2) {
     // ----------------------------------------------------------- producers
     // warp 0: K of each item, then the item's Q ring tiles (and the item
@@ -391,7 +400,9 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       have = advance();
       if (have) load();
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    if constexpr (C::REG_SOFT > 0) regs_claim<C::REG_SOFT>();
     // ------------------------------------------- softmax: P^T and dS^T
     const int wg = (warp - 4) >> 2;             // query columns [32 wg, 32 wg + 32)
     const int quarter = warp & 3;
@@ -561,6 +572,10 @@ struct DqCfg {
   static constexpr int OFF_MISC = OFF_CLC + 16 * kClcSlots;
   static constexpr int SMEM_BYTES = OFF_MISC + 16;  // base must be 1024-aligned (checked)
   static constexpr int THREADS = 128 + 128 * NWG;
+  // Registers per thread after the warpgroup split (0: no split); the launch
+  // must hold THREADS x launch registers >= REG_NEEDED (checked on the host).
+  static constexpr int REG_CTRL = 64, REG_SOFT = 104;
+  static constexpr int REG_NEEDED = REG_SOFT > 0 ? 128 * REG_CTRL + 128 * NWG * REG_SOFT : 0;
   static constexpr int S_COL = 0;
   static constexpr int DP_COL = 128;
   static constexpr int DQ_COL = 256;  // two accumulators, 128 columns apart
@@ -612,6 +627,9 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < 4) {
+  // producer / MMA warpgroup: registers handed to the softmax
+  if constexpr (C::REG_SOFT > 0) regs_release<C::REG_CTRL>();
   if (warp == 3) {
     // ------------------------------------------------ producer: Q and dO
     // once per item, each as soon as the previous item's last MMA reading it
@@ -770,7 +788,9 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     // every issued MMA completes before the CTA exits
     if (leader) mma_commit(bar(C::B_DRAIN));
     mbar_wait_poll(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
-  } else if (warp >= 4) {
+  }
+  } else {
+    if constexpr (C::REG_SOFT > 0) regs_claim<C::REG_SOFT>();
     const int wg = (warp - 4) >> 2;  // key columns [32 wg, 32 wg + 32)
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;

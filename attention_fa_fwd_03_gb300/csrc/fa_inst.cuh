@@ -3,6 +3,8 @@
 // stream. Each fa_inst_d*.cu picks the tile configuration for its head dim.
 #pragma once
 
+#include <type_traits>
+
 #include "fa_bwd.cuh"
 #include "fa_bwd_pipelined.cuh"
 #include "fa_fwd.cuh"
@@ -93,6 +95,16 @@ cudaError_t run_dvec(const BwdLaunch& a) {
   return cudaGetLastError();
 }
 
+// Kernel configurations without a register split need no check.
+template <class C, class = void>
+struct RegSplit {
+  static constexpr int needed = 0;
+};
+template <class C>
+struct RegSplit<C, std::void_t<decltype(C::REG_NEEDED)>> {
+  static constexpr int needed = C::REG_NEEDED;
+};
+
 template <class C, class Kern>
 cudaError_t launch_dkv_with(const BwdLaunch& a, Kern kern) {
   const int bhq = a.s.B * a.s.Hq, bhkv = a.s.B * a.s.Hkv;
@@ -105,6 +117,8 @@ cudaError_t launch_dkv_with(const BwdLaunch& a, Kern kern) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if (!register_split_fits(reinterpret_cast<const void*>(kern), C::THREADS, RegSplit<C>::needed))
+    return cudaErrorInvalidConfiguration;
   const TileOrder order = kv_block_order(a.s, C::D);
   kern<<<order.units * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream>>>(
       mq, mk, mv, mdo, a.lse, a.dvec, a.dk, a.dv, a.scale, a.s, order, a.wc);
@@ -123,6 +137,8 @@ cudaError_t launch_dq_with(const BwdLaunch& a, Kern kern) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if (!register_split_fits(reinterpret_cast<const void*>(kern), C::THREADS, RegSplit<C>::needed))
+    return cudaErrorInvalidConfiguration;
   const TileOrder order = query_block_order(a.s, kBM, C::D);
   kern<<<order.units * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream>>>(
       mq, mk, mv, mdo, a.lse, a.dvec, a.dq, a.scale, a.s, order, a.wc);
