@@ -108,6 +108,25 @@ def ncu_traffic(kernel: str, workload: str):
     return None
 
 
+# ------------------------------------------------------------- multi-rank
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest ``value`` over all ranks: a replicated job takes as long as
+    its slowest rank. Uses the default process group when ``world > 1``."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, steps: int, flops_per_step: float, max_total_ms: float) -> float:
+    """Whole-job TFLOP/s: each of ``world`` ranks runs ``steps`` full steps
+    (weak scaling), timed by the slowest rank."""
+    return world * steps * flops_per_step / (max_total_ms / 1e3) / 1e12
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -266,13 +285,9 @@ def run_ours(args, rank, world, local_rank):
 
     step_ms = [e[0].elapsed_time(e[4]) for e in evs]
     phase_ms = [[e[j].elapsed_time(e[j + 1]) for e in evs] for j in range(4)]
-    total_ms = sum(step_ms)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     fwd_f, bwd_f = counted_flops(w)
-    value = world * args.steps * (fwd_f + bwd_f) / (total_ms / 1e3) / 1e12
+    value = job_tflops(world, args.steps, fwd_f + bwd_f, total_ms)
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -303,12 +318,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         e1.record()
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / n_e2e
-        te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        if world > 1:
-            torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(te.item())
-        e2e = {"value": round(world * (fwd_f + bwd_f) / (e2e_ms / 1e3) / 1e12, 2),
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+        e2e = {"value": round(job_tflops(world, 1, fwd_f + bwd_f, e2e_ms), 2),
                "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "api": "fa_fwd + fa_bwd (C ABI via the Python binding), pinned host buffers"}
