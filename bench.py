@@ -129,7 +129,9 @@ def job_tflops(world: int, steps: int, flops_per_step: float, max_total_ms: floa
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 50 ms) of the SM clock and the throttle
+    reasons; only the samples taken inside [t0, t1] (wall clock) count."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
@@ -142,12 +144,45 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(self.idx)],
+                 "-lms", "50", "-i", str(self.idx)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
-    def stop(self) -> dict:
+    @staticmethod
+    def parse(out: str, t0: float, t1: float) -> dict:
+        import datetime
+        sm, mx, pw, reasons, outside = [], [], [], set(), 0
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, clk_max = float(parts[2]), float(parts[3])
+            except ValueError:
+                continue
+            if not (t0 <= ts <= t1):
+                outside += 1
+                continue
+            sm.append(clk)
+            mx.append(clk_max)
+            try:
+                pw.append(float(parts[4]))
+            except ValueError:
+                pass
+            for name, val in zip(ClockSampler.NAMES, parts[6:10]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"error": "no clock sample inside the timed region", "samples_outside": outside}
+        r = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "sm_min_mhz": min(sm),
+             "samples": len(sm), "reasons": sorted(reasons)}
+        if pw:
+            r["power_w_median"] = statistics.median(pw)
+        return r
+
+    def stop(self, t0: float, t1: float) -> dict:
         if self.proc is None:
             return {"error": "nvidia-smi unavailable"}
         self.proc.terminate()
@@ -156,23 +191,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        for line in out.splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(self.NAMES, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"error": "no clock samples"}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return self.parse(out, t0, t1)
 
 
 def physical_gpu_index(local_rank: int) -> int:
@@ -273,14 +292,16 @@ def run_ours(args, rank, world, local_rank):
     sampler.start()
     time.sleep(0.25)  # let the sampler start before the timed region
     wall0 = time.perf_counter()
+    t_region0 = time.time()
     for i in range(args.steps):
         flush.zero_()              # untimed: outside the step's event pair
         step(evs[i])
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    t_region1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(t_region0, t_region1)
     status = fa.fa_device_status()
 
     step_ms = [e[0].elapsed_time(e[4]) for e in evs]
@@ -439,7 +460,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=fa_inputs.HEADLINE, choices=sorted(fa_inputs.WORKLOADS))

@@ -56,3 +56,20 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.25, 1) == 3.25
     assert bench.job_tflops(1, 4, 1.0e12, 2.0) == pytest.approx(2000.0)
+
+
+def test_clock_sampler_keeps_only_samples_inside_the_timed_region():
+    import datetime
+    import bench
+    t0 = 1_800_000_000.0
+
+    def line(t, clk, hw="Not Active", cap="Not Active"):
+        ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, 0, {clk}, 2070, 1200.0, 0x0, {hw}, Not Active, Not Active, {cap}"
+
+    out = "\n".join([line(t0 - 0.5, 2070), line(t0 + 0.1, 1900, cap="Active"),
+                     line(t0 + 0.2, 1800), line(t0 + 0.3, 1850), line(t0 + 2.0, 345, hw="Active")])
+    r = bench.ClockSampler.parse(out, t0, t0 + 1.0)
+    assert r["samples"] == 3 and r["sm_mhz"] == 1850.0 and r["sm_min_mhz"] == 1800.0
+    assert r["reasons"] == ["sw_power_cap"]              # the hw_slowdown sample was outside
+    assert "error" in bench.ClockSampler.parse(out, t0 + 5, t0 + 6)
