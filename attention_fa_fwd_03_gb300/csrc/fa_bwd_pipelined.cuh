@@ -203,6 +203,9 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     // land under full load, so each ring is refilled the moment its own slot
     // frees. The whole warp runs the loop (a lone active lane whose siblings
     // wait at the final barrier issues far slower); one elected lane issues.
+    // Producers wait with try_wait (the warp sleeps in the barrier instead of
+    // taking issue slots from the softmax warps of its SM sub-partition); only
+    // the MMA issuer polls.
     const bool leader = elect_one_sync();
     const bool q_ring = warp == 0;
     if (leader) tma_prefetch_desc(q_ring ? &map_q : &map_do);
@@ -224,7 +227,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       const DkvItem t = dkv_item(item, order, s, C::BMQ);
       if (t.n_iter > 0) {
         // K (or V) of this KV block, once its previous contents were last read
-        if (ln > 0) ok = mbar_wait_poll(bar(once_empty), (ln - 1) & 1, tmo, abort_flag, wc.status);
+        if (ln > 0) ok = mbar_wait(bar(once_empty), (ln - 1) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         if (leader) mbar_arrive_expect_tx(bar(once_full), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
@@ -234,7 +237,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           const int zq = t.b * s.Hq + t.g * reps + it / t.n_qt;
           const int i0 = (t.i_lo + it % t.n_qt) * C::BMQ;
           const int st = gt % nst;
-          if (gt >= nst) ok = mbar_wait_poll(bar(empty + st), ((gt / nst) - 1) & 1, tmo, abort_flag, wc.status);
+          if (gt >= nst) ok = mbar_wait(bar(empty + st), ((gt / nst) - 1) & 1, tmo, abort_flag, wc.status);
           if (!ok) break;
           if (leader) mbar_arrive_expect_tx(bar(full + st), C::TILE);
           for (int r = 0; r < C::KREG; ++r)
@@ -347,7 +350,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     }
     // every issued MMA completes before the CTA exits
     if (leader) mma_commit(bar(C::B_DRAIN));
-    mbar_wait_poll(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
+    mbar_wait(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
   } else if (warp == 3) {
     // ------------------------------------------- LSE / D-vector staging
     // a flat stream over the tiles of the CTA's items; each lane loads its
@@ -640,13 +643,13 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     for (int k = 0, item = blockIdx.x; ok; ++k) {
       const DqItem t = dq_item(item, order, s, C::BN);
       if (t.n_iter > 0) {
-        if (ln > 0) ok = mbar_wait_poll(bar(C::B_QEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
+        if (ln > 0) ok = mbar_wait(bar(C::B_QEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
           if (leader) tma_load_3d(sbase + C::OFF_Q + r * C::REGION, &map_q, bar(C::B_QFULL), r * 64, t.q0, t.bh);
         ++nq;
-        if (ln > 0) ok = mbar_wait_poll(bar(C::B_DOEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
+        if (ln > 0) ok = mbar_wait(bar(C::B_DOEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         if (leader) mbar_arrive_expect_tx(bar(C::B_DOFULL), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
@@ -684,7 +687,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       for (int it = 0; it < t.n_iter; ++it, ++gt) {
         const int kr = (t.j_lo + it) * C::BN;
         const int st = gt % nst;
-        if (gt >= nst) ok = mbar_wait_poll(bar(empty + st), ((gt / nst) - 1) & 1, tmo, abort_flag, wc.status);
+        if (gt >= nst) ok = mbar_wait(bar(empty + st), ((gt / nst) - 1) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         if (leader) mbar_arrive_expect_tx(bar(full + st), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
@@ -787,7 +790,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     }
     // every issued MMA completes before the CTA exits
     if (leader) mma_commit(bar(C::B_DRAIN));
-    mbar_wait_poll(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
+    mbar_wait(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
   }
   } else {
     if constexpr (C::REG_SOFT > 0) regs_claim<C::REG_SOFT>();
