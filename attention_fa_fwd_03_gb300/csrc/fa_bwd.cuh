@@ -30,6 +30,8 @@ namespace fa {
 // ------------------------------------------------------------ pass 1: D-vector
 // One group of TPR threads per row; each thread reads 16 bytes of O and dO per
 // step (fully coalesced), fp32 accumulation, shuffle reduction in the group.
+// The loop bound is uniform over the block, so every lane of a warp reaches
+// every shuffle (a row past the end loads zeros and stores nothing).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
 fa_bwd_dvec_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
@@ -39,10 +41,13 @@ fa_bwd_dvec_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
   constexpr int ROWS_PER_BLOCK = 256 / TPR;
   const int sub = threadIdx.x % TPR;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * ROWS_PER_BLOCK;
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * ROWS_PER_BLOCK + threadIdx.x / TPR;
-       row < nrows; row += stride) {
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * ROWS_PER_BLOCK; base < nrows;
+       base += stride) {
+    const int64_t row = base + threadIdx.x / TPR;
+    const bool valid = row < nrows;
     float acc = 0.f;
     for (int ch = sub; ch < CHUNKS; ch += TPR) {
+      if (!valid) break;
       const uint4 a = __ldg(o + row * CHUNKS + ch);
       const uint4 b = __ldg(dout + row * CHUNKS + ch);
       const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
@@ -57,7 +62,7 @@ fa_bwd_dvec_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
     }
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (sub == 0) dvec[row] = acc;
+    if (sub == 0 && valid) dvec[row] = acc;
   }
 }
 

@@ -204,45 +204,59 @@ def physical_gpu_index(local_rank: int) -> int:
 
 
 # ------------------------------------------------------------ CPU baseline
-def oracle_sample(w, target_s: float):
-    """Time the oracle (fwd + bwd) on one (batch, KV group) slice, query rows
-    [Tq - R, Tq), R sized to take about ``target_s`` seconds. Returns
-    (seconds per full step, cores, description)."""
-    import oracle
-    import numpy as np
-    reps = w.Hq // w.Hkv
-    x = fa_inputs.make_inputs(w)
-    # batch 0, KV group 0 and its reps query heads: an independent sub-problem
-    xs = [x["q"][0:1, 0:reps], x["k"][0:1, 0:1], x["v"][0:1, 0:1], x["do"][0:1, 0:reps]]
-    xs = [t.double().numpy() for t in xs]
-    total_pairs = w.B * w.Hq * visible_pairs_per_head(w)
+class OracleSample:
+    """The oracle (fwd + bwd) on one (batch, KV group) slice of the workload:
+    all its query heads, query rows [Tq - R, Tq) with R sized to take about a
+    target time; the time per full step is extrapolated by visible pairs. The
+    slice's inputs are generated once (the same seeded bits as the GPU run)."""
 
-    def run(rows):
+    def __init__(self, w):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        self.reps = w.Hq // w.Hkv
+        x = fa_inputs.make_inputs(w)
+        xs = [x["q"][0:1, 0:self.reps], x["k"][0:1, 0:1], x["v"][0:1, 0:1], x["do"][0:1, 0:self.reps]]
+        self.xs = [t.double().numpy() for t in xs]
+        self.total_pairs = w.B * w.Hq * visible_pairs_per_head(w)
+        self.per_pair = None
+
+    def run(self, rows):
+        w = self.w
         lo = w.Tq - rows
         t0 = time.perf_counter()
-        oracle.attn_fwd(*xs[:3], w.scale, w.causal, w.window, row_lo=lo, row_hi=w.Tq)
-        oracle.attn_bwd(*xs, w.scale, w.causal, w.window, row_lo=lo, row_hi=w.Tq)
-        dt = time.perf_counter() - t0
-        return dt, reps * visible_pairs_per_head(w, (lo, w.Tq))
+        self.oracle.attn_fwd(*self.xs[:3], w.scale, w.causal, w.window, row_lo=lo, row_hi=w.Tq)
+        self.oracle.attn_bwd(*self.xs, w.scale, w.causal, w.window, row_lo=lo, row_hi=w.Tq)
+        return time.perf_counter() - t0, self.reps * visible_pairs_per_head(w, (lo, w.Tq))
 
-    rows = min(w.Tq, 8)
-    dt, pairs = run(rows)
-    per_pair = dt / max(pairs, 1)
-    full_rows_pairs = reps * visible_pairs_per_head(w)
-    want_pairs = target_s / per_pair
-    if want_pairs >= full_rows_pairs:
-        rows = w.Tq
-    else:
-        lo_rows = 8
-        while lo_rows < w.Tq and reps * visible_pairs_per_head(w, (w.Tq - lo_rows, w.Tq)) < want_pairs:
-            lo_rows *= 2
-        rows = min(lo_rows, w.Tq)
-    dt, pairs = run(rows)
-    per_step = dt * total_pairs / pairs
-    desc = (f"one (batch, KV group) slice ({reps} of {w.B * w.Hq} query heads), query rows "
-            f"[{w.Tq - rows}, {w.Tq}): {pairs} of {total_pairs} visible pairs, fwd + bwd "
-            f"in {dt:.2f} s, extrapolated by visible pairs")
-    return per_step, oracle.num_threads(), desc, dt
+    def rows_for(self, target_s: float) -> int:
+        w = self.w
+        if self.per_pair is None:
+            dt, pairs = self.run(min(w.Tq, 8))
+            self.per_pair = dt / max(pairs, 1)
+        want_pairs = target_s / self.per_pair
+        rows = min(w.Tq, 8)
+        while rows < w.Tq and self.reps * visible_pairs_per_head(w, (w.Tq - rows, w.Tq)) < want_pairs:
+            rows *= 2
+        return min(rows, w.Tq)
+
+    def step(self, target_s: float):
+        """(seconds per full step, seconds spent, description)."""
+        rows = self.rows_for(target_s)
+        dt, pairs = self.run(rows)
+        per_step = dt * self.total_pairs / pairs
+        desc = (f"one (batch, KV group) slice ({self.reps} of {self.w.B * self.w.Hq} query heads), "
+                f"query rows [{self.w.Tq - rows}, {self.w.Tq}): {pairs} of {self.total_pairs} visible "
+                f"pairs, fwd + bwd in {dt:.2f} s, extrapolated by visible pairs")
+        return per_step, dt, desc
+
+
+def oracle_sample(w, target_s: float):
+    """Time the oracle on a bounded sample of the workload (OracleSample):
+    (seconds per full step, cores, description, seconds spent)."""
+    smp = OracleSample(w)
+    per_step, dt, desc = smp.step(target_s)
+    return per_step, smp.oracle.num_threads(), desc, dt
 
 
 # ---------------------------------------------------------------- our path
@@ -430,18 +444,22 @@ def run_ours(args, rank, world, local_rank):
 
 # ----------------------------------------------------------- reference arm
 def run_reference(args):
-    import oracle
+    """The oracle as the reference arm: each of warm-up + timed steps runs a
+    bounded sample of the workload (sized so the whole run takes about two
+    minutes), extrapolated to a full step."""
     w = fa_inputs.WORKLOADS[args.workload]
     fwd_f, bwd_f = counted_flops(w)
-    budget = max(5.0, 150.0 / max(1, args.steps + args.warmup))
+    smp = OracleSample(w)
+    budget = max(0.05, 120.0 / max(1, args.steps + args.warmup))
     per_step = []
-    desc = cores = None
+    desc = None
     for i in range(args.warmup + args.steps):
-        s, cores, desc, took = oracle_sample(w, budget)
+        s, _, desc = smp.step(budget)
         if i >= args.warmup:
             per_step.append(s)
     mean_s = sum(per_step) / len(per_step)
     value = (fwd_f + bwd_f) / mean_s / 1e12
+    cores = smp.oracle.num_threads()
     return {
         "metric": "attention fwd+bwd TFLOP/s at 1 GB300 (and % of dense bf16 peak)",
         "impl": "reference", "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
