@@ -216,6 +216,9 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const uint32_t once = sbase + (q_ring ? C::OFF_K : C::OFF_V);
     const CUtensorMap* map = q_ring ? &map_q : &map_do;
     const CUtensorMap* once_map = q_ring ? &map_k : &map_v;
+    // Q / dO tiles are read by every KV block of the group: keep them in L2;
+    // each K / V block is read once
+    const uint64_t pol_ring = l2_policy_evict_last(), pol_once = l2_policy_evict_first();
     int gt = 0, ln = 0, asked = 0;  // ring tiles issued, items with work, item requests
     bool ok = true;
     for (int k = 0, item = blockIdx.x; ok; ++k) {
@@ -231,7 +234,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (!ok) break;
         if (leader) mbar_arrive_expect_tx(bar(once_full), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(once + r * C::REGION, once_map, bar(once_full), r * 64, t.k0, t.bg);
+          if (leader) tma_load_3d_hint(once + r * C::REGION, once_map, bar(once_full), r * 64, t.k0, t.bg, pol_once);
         ++ln;
         for (int it = 0; it < t.n_iter; ++it, ++gt) {
           const int zq = t.b * s.Hq + t.g * reps + it / t.n_qt;
@@ -241,7 +244,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           if (!ok) break;
           if (leader) mbar_arrive_expect_tx(bar(full + st), C::TILE);
           for (int r = 0; r < C::KREG; ++r)
-            if (leader) tma_load_3d(ring + st * C::TILE + r * C::REGION, map, bar(full + st), r * 64, i0, zq);
+            if (leader) tma_load_3d_hint(ring + st * C::TILE + r * C::REGION, map, bar(full + st), r * 64, i0, zq, pol_ring);
         }
         if (!ok) break;
       }
@@ -636,8 +639,9 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   if (warp == 3) {
     // ------------------------------------------------ producer: Q and dO
     // once per item, each as soon as the previous item's last MMA reading it
-    // (its last S, its last dP) completes
+    // (its last S, its last dP) completes; read once, so not kept in L2
     const bool leader = elect_one_sync();
+    const uint64_t pol_once = l2_policy_evict_first();
     int ln = 0, nq = 0, ndo = 0;  // items with work; Q, dO loads issued
     bool ok = true;
     for (int k = 0, item = blockIdx.x; ok; ++k) {
@@ -647,13 +651,13 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         if (!ok) break;
         if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(sbase + C::OFF_Q + r * C::REGION, &map_q, bar(C::B_QFULL), r * 64, t.q0, t.bh);
+          if (leader) tma_load_3d_hint(sbase + C::OFF_Q + r * C::REGION, &map_q, bar(C::B_QFULL), r * 64, t.q0, t.bh, pol_once);
         ++nq;
         if (ln > 0) ok = mbar_wait(bar(C::B_DOEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         if (leader) mbar_arrive_expect_tx(bar(C::B_DOFULL), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(sbase + C::OFF_DO + r * C::REGION, &map_do, bar(C::B_DOFULL), r * 64, t.q0, t.bh);
+          if (leader) tma_load_3d_hint(sbase + C::OFF_DO + r * C::REGION, &map_do, bar(C::B_DOFULL), r * 64, t.q0, t.bh, pol_once);
         ++ndo;
         ++ln;
       }
@@ -674,6 +678,9 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const int full = k_ring ? C::B_KFULL : C::B_VFULL, empty = k_ring ? C::B_KEMPTY : C::B_VEMPTY;
     const uint32_t ring = sbase + (k_ring ? C::OFF_K : C::OFF_V);
     const CUtensorMap* map = k_ring ? &map_k : &map_v;
+    // K / V tiles are read by every query block of the group's heads: keep
+    // them in L2
+    const uint64_t pol_ring = l2_policy_evict_last();
     int gt = 0, asked = 0;
     bool ok = true;
     for (int k = 0, item = blockIdx.x; ok; ++k) {
@@ -691,7 +698,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         if (!ok) break;
         if (leader) mbar_arrive_expect_tx(bar(full + st), C::TILE);
         for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d(ring + st * C::TILE + r * C::REGION, map, bar(full + st), r * 64, kr, zkv);
+          if (leader) tma_load_3d_hint(ring + st * C::TILE + r * C::REGION, map, bar(full + st), r * 64, kr, zkv, pol_ring);
       }
       if (!ok) break;
       if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;

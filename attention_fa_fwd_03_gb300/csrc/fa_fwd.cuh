@@ -153,6 +153,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     if (leader) tma_prefetch_desc(&map_q);
     if (leader) tma_prefetch_desc(&map_k);
     if (leader) tma_prefetch_desc(&map_v);
+    // K / V tiles are read by every query block of the group's heads: keep
+    // them in L2; each Q block is read once
+    const uint64_t pol_kv = l2_policy_evict_last(), pol_q = l2_policy_evict_first();
     int gk = 0, ln = 0, asked = 0;  // ring tiles issued, blocks with work, requests
     bool ok = true;
     for (int k = 0, item = blockIdx.x; ok; ++k) {
@@ -167,8 +170,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         for (int tq = 0; tq < C::NQ; ++tq)
           for (int r = 0; r < C::KREG; ++r)
             if (leader)
-              tma_load_3d(sbase + C::OFF_Q + tq * C::Q_TILE + r * C::Q_REGION, &map_q, bar(C::B_QFULL),
-                          r * 64, t.q0 + tq * kBM, t.bh);
+              tma_load_3d_hint(sbase + C::OFF_Q + tq * C::Q_TILE + r * C::Q_REGION, &map_q, bar(C::B_QFULL),
+                               r * 64, t.q0 + tq * kBM, t.bh, pol_q);
         ++ln;
         const int zkv = t.b * s.Hkv + t.g;
         for (int it = 0; it < t.n_iter; ++it, ++gk) {
@@ -180,13 +183,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           if (leader) mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::KV_TILE);
           for (int r = 0; r < C::KREG; ++r)
             if (leader)
-              tma_load_3d(sbase + C::OFF_K + st * C::KV_TILE + r * C::KV_REGION, &map_k,
-                          bar(C::B_KFULL + st), r * 64, krow, zkv);
+              tma_load_3d_hint(sbase + C::OFF_K + st * C::KV_TILE + r * C::KV_REGION, &map_k,
+                               bar(C::B_KFULL + st), r * 64, krow, zkv, pol_kv);
           if (leader) mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::KV_TILE);
           for (int r = 0; r < C::KREG; ++r)
             if (leader)
-              tma_load_3d(sbase + C::OFF_V + st * C::KV_TILE + r * C::KV_REGION, &map_v,
-                          bar(C::B_VFULL + st), r * 64, krow, zkv);
+              tma_load_3d_hint(sbase + C::OFF_V + st * C::KV_TILE + r * C::KV_REGION, &map_v,
+                               bar(C::B_VFULL + st), r * 64, krow, zkv, pol_kv);
         }
         if (!ok) break;
       }
