@@ -15,10 +15,12 @@
 //   expensive part), while the tensor core is still busy with the previous
 //   tile's accumulating MMAs and this tile's dP. Only dS = P o (dP - D) waits
 //   for dP(i); P and dS (16-bit) are then written over the dP columns.
-// * The score columns are free once the softmax has read them, so S(i+1) is
-//   issued then. Per tile the tensor core runs, back to back:
-//     dK/dV:  S^T(i+1)  dK,dV += (dS^T, P^T)(i) . (Q, dO)(i)  dP^T(i+1)
-//     dQ:     S(j+1)    dQ += dS(j) K(j)                        dP(j+1)
+// * dK/dV: P^T is written over the score columns it came from as soon as
+//   the exponentials are done, so dV(i) and the next S^T run while dP^T(i)
+//   and dS^T are still in progress; dK(i) follows when dS^T(i) is in TMEM:
+//     S^T(i+1) after dV(i),  dK(i) after dS^T(i),  dP^T(i+1) after dK(i)
+//   dQ: the score columns are free once the softmax has read them, so S(j+1)
+//   is issued then:  S(j+1)  dQ += dS(j) K(j)  dP(j+1)
 // * The operand the next tile needs first (Q in dK/dV, K in dQ) is
 //   prefetched three tiles deep, the other two deep, each slot released by
 //   the MMA that last reads it.
@@ -36,13 +38,13 @@
 //   release the next item's first P/dS block.
 // NWG softmax warpgroups split the 128 columns of every tile (128 / NWG each).
 //
-// TMEM layout of the 16-bit operands (written over the dP block they derive
-// from). dK/dV: the 16 query columns of K-block kk of the accumulating MMAs
-// come from dP^T columns DP_COL + 16 kk ..; their P^T (8 columns of packed
-// pairs) goes to DP_COL + 16 kk and their dS^T to DP_COL + 16 kk + 8, so each
-// 16-column half is read, then overwritten. dQ: the score columns are handled
-// in chunks of 32; chunk m (from dP columns DP_COL + 32m ..) writes its dS to
-// [+0, +16), so K-block kk reads DP_COL + 32 (kk / 2) + 8 (kk % 2).
+// TMEM layout of the 16-bit operands: the score columns are handled in chunks
+// of 32 (one per softmax warpgroup); chunk m writes its 16-bit result packed
+// into the first 16 columns of the chunk it was read from. dK/dV: P^T into
+// S^T chunk m, dS^T into dP^T chunk m (dP^T is read in two 16-column halves,
+// each half's 8 result columns landing in columns already read); dQ: dS into
+// dP chunk m. So K-block kk of the next MMA reads column base + 32 (kk / 2) +
+// 8 (kk % 2).
 #pragma once
 
 #include <type_traits>
@@ -116,13 +118,13 @@ struct DkvCfg {
   static constexpr int OFF_STATS = OFF_DO + DST * TILE;  // [2][-lse2 | -dvec][128] fp32
   static constexpr int OFF_BAR = OFF_STATS + 2 * 2 * BMQ * 4;
   // barriers: k_full, k_empty, v_full, v_empty, q_full[QST], q_empty[QST],
-  // do_full[DST], do_empty[DST], stats_full[2], stats_empty[2], s_full, s_free,
-  // dp_full, p_full, done, drain
+  // do_full[DST], do_empty[DST], stats_full[2], stats_empty[2], s_full,
+  // ds_ready, dp_full, p_ready, done, drain
   static constexpr int B_KFULL = 0, B_KEMPTY = 1, B_VFULL = 2, B_VEMPTY = 3, B_QFULL = 4,
                        B_QEMPTY = B_QFULL + QST, B_DOFULL = B_QEMPTY + QST,
                        B_DOEMPTY = B_DOFULL + DST, B_STFULL = B_DOEMPTY + DST,
-                       B_STEMPTY = B_STFULL + 2, B_SFULL = B_STEMPTY + 2, B_SFREE = B_SFULL + 1,
-                       B_DPFULL = B_SFULL + 2, B_PFULL = B_SFULL + 3, B_DONE = B_SFULL + 4,
+                       B_STEMPTY = B_STFULL + 2, B_SFULL = B_STEMPTY + 2, B_DSREADY = B_SFULL + 1,
+                       B_DPFULL = B_SFULL + 2, B_PREADY = B_SFULL + 3, B_DONE = B_SFULL + 4,
                        B_DRAIN = B_SFULL + 5, B_CLCFULL = B_DRAIN + 1,
                        B_CLCEMPTY = B_CLCFULL + kClcSlots, NBAR = B_CLCEMPTY + kClcSlots;
   static constexpr int OFF_CLC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // item responses
@@ -139,8 +141,8 @@ struct DkvCfg {
   static constexpr int DP_COL = 128;  // dP^T block, 128 fp32 columns
   static constexpr int DV_COL = 256;
   static constexpr int DK_COL = 256 + D;
-  static constexpr uint32_t pt_col(int kk) { return DP_COL + 16 * kk; }
-  static constexpr uint32_t dst_col(int kk) { return DP_COL + 16 * kk + 8; }
+  static constexpr uint32_t pt_col(int kk) { return chunk_operand_col(S_COL, kk); }
+  static constexpr uint32_t dst_col(int kk) { return chunk_operand_col(DP_COL, kk); }
   static_assert(NWG == 4, "one 32-column chunk per softmax warpgroup");
   static_assert(D <= 128, "dV and dK accumulators share 256 TMEM columns");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -177,7 +179,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
       if (i == C::B_STFULL || i == C::B_STFULL + 1) cnt = 32;  // the staging warp's lanes
-      if (i == C::B_STEMPTY || i == C::B_STEMPTY + 1 || i == C::B_SFREE || i == C::B_PFULL)
+      if (i == C::B_STEMPTY || i == C::B_STEMPTY + 1 || i == C::B_DSREADY || i == C::B_PREADY)
         cnt = 4 * C::NWG;  // one arrival per softmax warp
       if (i >= C::B_CLCEMPTY && i < C::B_CLCEMPTY + kClcSlots) cnt = C::THREADS / 32;
       mbar_init(bar(i), cnt);
@@ -282,17 +284,16 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       const DkvItem t = dkv_item(item, order, s, C::BMQ);
       const int n = t.n_iter;
       if (n > 0) {
-        // S^T of the item's first tile: its K block, Q(gt), and the softmax
-        // done reading the previous S^T
-        ok = wait(C::B_KFULL, ln) && wait(C::B_QFULL + gt % C::QST, gt / C::QST) &&
-             (gt == 0 || wait(C::B_SFREE, gt - 1));
+        // S^T of the item's first tile: its K block and Q(gt) (the score
+        // columns were last read by the previous tile's dV, issued before)
+        ok = wait(C::B_KFULL, ln) && wait(C::B_QFULL + gt % C::QST, gt / C::QST);
         if (!ok) break;
         tc_fence_after();
         if (leader) issue_score(sbase + C::OFF_K, sbase + C::OFF_Q + (gt % C::QST) * C::TILE, C::S_COL);
         if (leader) mma_commit(bar(C::B_SFULL));
         if (n == 1 && leader) mma_commit(bar(C::B_KEMPTY));  // K read for the last time
-        // dP^T of the first tile (over the P^T / dS^T columns of the previous
-        // tile, whose MMAs precede it in issue order)
+        // dP^T of the first tile (over the dS^T columns of the previous tile,
+        // whose dK precedes it in issue order)
         ok = wait(C::B_VFULL, ln) && wait(C::B_DOFULL + gt % C::DST, gt / C::DST);
         if (!ok) break;
         tc_fence_after();
@@ -303,38 +304,40 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           const int gi = gt + it;
           const int qs = gi % C::QST, ds = gi % C::DST;
           const bool more = it + 1 < n;
-          if (more) {
-            // next S^T as soon as the softmax has read this tile's S^T
-            const int nq = (gi + 1) % C::QST;
-            ok = wait(C::B_QFULL + nq, (gi + 1) / C::QST) && wait(C::B_SFREE, gi);
-            if (!ok) break;
-            tc_fence_after();
-            if (leader) issue_score(sbase + C::OFF_K, sbase + C::OFF_Q + nq * C::TILE, C::S_COL);
-            if (leader) mma_commit(bar(C::B_SFULL));
-            if (it + 2 == n && leader) mma_commit(bar(C::B_KEMPTY));
-          }
-          // P^T / dS^T of this tile in TMEM; for the item's first tile this
-          // also means the softmax warps have stored the previous item's dK, dV
-          ok = wait(C::B_PFULL, gi);
+          // dV += P^T dO once P^T(it) is in TMEM (A from TMEM, B MN-major, K =
+          // query rows); for the item's first tile this also means the softmax
+          // warps have stored the previous item's dK, dV. dO(it) is then free.
+          ok = wait(C::B_PREADY, gi);
           if (!ok) break;
           tc_fence_after();
-          // dK += dS^T Q, then dV += P^T dO  (A from TMEM, B MN-major, K = query
-          // rows); each ring slot is released by the last MMA that reads it
-          const uint64_t qdesc = make_sdesc(sbase + C::OFF_Q + qs * C::TILE, C::REGION, 1024, 2);
           const uint64_t ddesc = make_sdesc(sbase + C::OFF_DO + ds * C::TILE, C::REGION, 1024, 2);
-#pragma unroll
-          for (int kk = 0; kk < C::BMQ / 16; ++kk)
-            if (leader) mma_ts(tmem + C::DK_COL, tmem + C::dst_col(kk), qdesc + ((kk * 16 * 128) >> 4),
-                               idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
-          if (leader) mma_commit(bar(C::B_QEMPTY + qs));
 #pragma unroll
           for (int kk = 0; kk < C::BMQ / 16; ++kk)
             if (leader) mma_ts(tmem + C::DV_COL, tmem + C::pt_col(kk), ddesc + ((kk * 16 * 128) >> 4),
                                idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
           if (leader) mma_commit(bar(C::B_DOEMPTY + ds));
           if (more) {
-            // dP^T(it+1) overwrites the P^T / dS^T columns the MMAs above read
-            // (tcgen05 MMAs of one thread execute in order)
+            // next S^T over the P^T columns dV has just read (in issue order)
+            const int nq = (gi + 1) % C::QST;
+            ok = wait(C::B_QFULL + nq, (gi + 1) / C::QST);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) issue_score(sbase + C::OFF_K, sbase + C::OFF_Q + nq * C::TILE, C::S_COL);
+            if (leader) mma_commit(bar(C::B_SFULL));
+            if (it + 2 == n && leader) mma_commit(bar(C::B_KEMPTY));
+          }
+          // dK += dS^T Q once dS^T(it) is in TMEM; Q(it) is then free
+          ok = wait(C::B_DSREADY, gi);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t qdesc = make_sdesc(sbase + C::OFF_Q + qs * C::TILE, C::REGION, 1024, 2);
+#pragma unroll
+          for (int kk = 0; kk < C::BMQ / 16; ++kk)
+            if (leader) mma_ts(tmem + C::DK_COL, tmem + C::dst_col(kk), qdesc + ((kk * 16 * 128) >> 4),
+                               idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          if (leader) mma_commit(bar(C::B_QEMPTY + qs));
+          if (more) {
+            // dP^T(it+1) over the dS^T columns dK has just read (in issue order)
             const int nd = (gi + 1) % C::DST;
             ok = wait(C::B_DOFULL + nd, (gi + 1) / C::DST);
             if (!ok) break;
@@ -431,11 +434,9 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (!ok) break;
         tc_fence_after();
         uint32_t sv[32];
-        tmem_ld32(tmem + lane_base + C::S_COL + wg * C::CW, sv);
+        const uint32_t s_chunk = tmem + lane_base + C::S_COL + wg * C::CW;
+        tmem_ld32(s_chunk, sv);
         tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_SFREE));  // the next S^T may overwrite them
         const float* nl_s = stats + slot * 2 * C::BMQ + wg * C::CW;  // -LSE * log2(e)
         const float* nd_s = nl_s + C::BMQ;                           // -D
         if (!block_unmasked(s, i0, i0 + C::BMQ, t.k0, t.k0 + kBM)) {
@@ -446,14 +447,27 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             sv[q] = (q >= lo && q < hi) ? sv[q] : __float_as_uint(-INFINITY);
         }
         exp2_scores32(sv, c2, nl_s, true, 0);  // sv now holds P (fp32)
+        {
+          // P^T (16-bit) over this chunk's S^T columns, for dV right away
+          uint32_t pp[16];
+#pragma unroll
+          for (int q = 0; q < 32; q += 2)
+            pp[q / 2] = pack2<C::BF16>(__uint_as_float(sv[q]), __uint_as_float(sv[q + 1]));
+          tmem_st16(s_chunk, pp);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::B_PREADY));
+        }
         // dS^T = P^T o (dP^T - D) once dP^T(it) is in TMEM
         ok = mbar_wait(bar(C::B_DPFULL), gi & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         tc_fence_after();
-        // two 16-column halves: load dP^T, then write [P^T | dS^T] over it
+        // two 16-column halves: load dP^T, then write 8 columns of dS^T into
+        // columns already read
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t pv[16], w[16];
+          uint32_t pv[16], w[8];
           tmem_ld16(tmem + lane_base + col + 16 * h, pv);
           tmem_ld_wait();
 #pragma unroll
@@ -467,17 +481,16 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                   f2_pack(__uint_as_float(pv[k + e]), __uint_as_float(pv[k + e + 1])),
                   e == 0 ? nd.x : nd.y);
               const float2 d2 = f2_unpack(fmul2(d, p2));
-              w[(k + e) / 2] = pack2<C::BF16>(__uint_as_float(sv[q]), __uint_as_float(sv[q + 1]));
-              w[8 + (k + e) / 2] = pack2<C::BF16>(d2.x, d2.y);
+              w[(k + e) / 2] = pack2<C::BF16>(d2.x, d2.y);
             }
           }
-          tmem_st16(tmem + lane_base + col + 16 * h, w);
+          tmem_st8(tmem + lane_base + col + 8 * h, w);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar(C::B_PFULL));
+          mbar_arrive(bar(C::B_DSREADY));
           mbar_arrive(bar(C::B_STEMPTY + slot));
         }
       }
