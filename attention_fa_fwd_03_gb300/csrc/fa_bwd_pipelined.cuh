@@ -20,7 +20,8 @@
 //   and dS^T are still in progress; dK(i) follows when dS^T(i) is in TMEM:
 //     S^T(i+1) after dV(i),  dK(i) after dS^T(i),  dP^T(i+1) after dK(i)
 //   dQ: the score columns are free once the softmax has read them, so S(j+1)
-//   is issued then:  S(j+1)  dQ += dS(j) K(j)  dP(j+1)
+//   is issued then; dP alternates between two TMEM blocks, so dP(j+1) need not
+//   wait for dQ(j) to read dS(j):  S(j+1)  dP(j+1)  dQ += dS(j) K(j)
 // * The operand the next tile needs first (Q in dK/dV, K in dQ) is
 //   prefetched three tiles deep, the other two deep, each slot released by
 //   the MMA that last reads it.
@@ -32,10 +33,10 @@
 //   between items, so the next item's first score block is computed while
 //   the softmax warps still finish (and store) the previous one; the operand
 //   loaded once per item (K, V in dK/dV; Q, dO in dQ) is reloaded as soon as
-//   the item's last MMA that reads it completes. dQ alternates between two
-//   TMEM accumulators so its store overlaps the next item; the dK/dV
-//   accumulators fill TMEM, and the softmax warps store them before they
-//   release the next item's first P/dS block.
+//   the item's last MMA that reads it completes. The softmax warps store an
+//   item's accumulators (dK, dV or dQ) before they release the next item's
+//   first P/dS block, which orders the store before that item's first
+//   accumulating MMA.
 // NWG softmax warpgroups split the 128 columns of every tile (128 / NWG each).
 //
 // TMEM layout of the 16-bit operands: the score columns are handled in chunks
@@ -43,8 +44,8 @@
 // into the first 16 columns of the chunk it was read from. dK/dV: P^T into
 // S^T chunk m, dS^T into dP^T chunk m (dP^T is read in two 16-column halves,
 // each half's 8 result columns landing in columns already read); dQ: dS into
-// dP chunk m. So K-block kk of the next MMA reads column base + 32 (kk / 2) +
-// 8 (kk % 2).
+// chunk m of the dP block it came from. So K-block kk of the next MMA reads
+// column base + 32 (kk / 2) + 8 (kk % 2).
 #pragma once
 
 #include <type_traits>
@@ -578,13 +579,12 @@ struct DqCfg {
   static constexpr int OFF_V = OFF_K + KST * TILE;
   static constexpr int OFF_BAR = OFF_V + VST * TILE;
   // barriers: q_full, q_empty, do_full, do_empty, k_full[KST], k_empty[KST],
-  // v_full[VST], v_empty[VST], s_full, s_free, dp_full, p_full, done[2],
-  // acc_free[2], drain
+  // v_full[VST], v_empty[VST], s_full, s_free, dp_full[2], p_full, done, drain
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_DOFULL = 2, B_DOEMPTY = 3, B_KFULL = 4,
                        B_KEMPTY = B_KFULL + KST, B_VFULL = B_KEMPTY + KST,
                        B_VEMPTY = B_VFULL + VST, B_SFULL = B_VEMPTY + VST,
-                       B_SFREE = B_SFULL + 1, B_DPFULL = B_SFULL + 2, B_PFULL = B_SFULL + 3,
-                       B_DONE = B_SFULL + 4, B_ACCFREE = B_DONE + 2, B_DRAIN = B_ACCFREE + 2,
+                       B_SFREE = B_SFULL + 1, B_DPFULL = B_SFULL + 2, B_PFULL = B_SFULL + 4,
+                       B_DONE = B_SFULL + 5, B_DRAIN = B_DONE + 1,
                        B_CLCFULL = B_DRAIN + 1, B_CLCEMPTY = B_CLCFULL + kClcSlots,
                        NBAR = B_CLCEMPTY + kClcSlots;
   static constexpr int OFF_CLC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // item responses
@@ -596,15 +596,20 @@ struct DqCfg {
   static constexpr int REG_CTRL = 64, REG_SOFT = 104;
   static constexpr int REG_NEEDED = REG_SOFT > 0 ? 128 * REG_CTRL + 128 * NWG * REG_SOFT : 0;
   static constexpr int S_COL = 0;
-  static constexpr int DP_COL = 128;
-  static constexpr int DQ_COL = 256;  // two accumulators, 128 columns apart
-  static constexpr uint32_t ds_col(int kk) { return chunk_operand_col(DP_COL, kk); }
+  static constexpr int DP_COL0 = 128;  // two dP blocks, 128 columns apart
+  static constexpr int DQ_COL = 384;   // one dQ accumulator
+  static constexpr uint32_t dp_col(int b) { return DP_COL0 + 128 * b; }
+  static constexpr uint32_t ds_col(int b, int kk) { return chunk_operand_col(dp_col(b), kk); }
   static_assert(NWG == 4, "one 32-column chunk per softmax warpgroup");
-  static_assert(D <= 128, "dQ accumulators in TMEM columns 256-383 and 384-511");
+  static_assert(D <= 128, "dQ accumulator in TMEM columns 384-511");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// Persistent like the dK/dV kernel above.
+// Two dP blocks in TMEM and one dQ accumulator: dP(j+1) is computed while the
+// softmax still turns dP(j) into dS(j), so the tensor core runs S(j+1),
+// dP(j+1), dQ(j) without waiting for dQ(j) to read dS. The item's dQ store is
+// ordered before the next item's first dQ by the softmax warps' next dS
+// arrival (as in dK/dV). Persistent like the dK/dV kernel above.
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
 fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -630,8 +635,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     *abort_flag = 0;
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == C::B_PFULL || i == C::B_SFREE || i == C::B_ACCFREE || i == C::B_ACCFREE + 1)
-        cnt = 4 * C::NWG;  // one arrival per softmax warp
+      if (i == C::B_PFULL || i == C::B_SFREE) cnt = 4 * C::NWG;  // one arrival per softmax warp
       if (i >= C::B_CLCEMPTY && i < C::B_CLCEMPTY + kClcSlots) cnt = C::THREADS / 32;
       mbar_init(bar(i), cnt);
     }
@@ -743,8 +747,6 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       const DqItem t = dq_item(item, order, s, C::BN);
       const int n = t.n_iter;
       if (n > 0) {
-        const int buf = ln & 1;
-        const uint32_t dq_col = C::DQ_COL + 128 * buf;
         // S of the item's first tile: its Q, K(gt), and the softmax done
         // reading the previous S
         ok = wait(C::B_QFULL, ln) && wait(C::B_KFULL + gt % C::KST, gt / C::KST) &&
@@ -754,18 +756,15 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         if (leader) issue_score(sbase + C::OFF_Q, sbase + C::OFF_K + (gt % C::KST) * C::TILE, C::S_COL);
         if (leader) mma_commit(bar(C::B_SFULL));
         if (n == 1 && leader) mma_commit(bar(C::B_QEMPTY));  // Q read for the last time
-        // dP of the first tile (over the dS columns of the previous tile, whose
-        // dQ MMAs precede it in issue order)
+        // dP of the first tile into block gt % 2 (its dS of two tiles back was
+        // read by a dQ issued before)
         ok = wait(C::B_DOFULL, ln) && wait(C::B_VFULL + gt % C::VST, gt / C::VST);
         if (!ok) break;
         tc_fence_after();
-        if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V + (gt % C::VST) * C::TILE, C::DP_COL);
-        if (leader) mma_commit(bar(C::B_DPFULL));
+        if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V + (gt % C::VST) * C::TILE, C::dp_col(gt & 1));
+        if (leader) mma_commit(bar(C::B_DPFULL + (gt & 1)));
         if (leader) mma_commit(bar(C::B_VEMPTY + gt % C::VST));  // V is read by dP only
         if (n == 1 && leader) mma_commit(bar(C::B_DOEMPTY));
-        // this accumulator's previous item has been stored
-        if (ln >= 2) ok = wait(C::B_ACCFREE + buf, (ln >> 1) - 1);
-        if (!ok) break;
         for (int it = 0; it < n; ++it) {
           const int gi = gt + it;
           const int ks = gi % C::KST;
@@ -778,7 +777,18 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             if (leader) issue_score(sbase + C::OFF_Q, sbase + C::OFF_K + nk * C::TILE, C::S_COL);
             if (leader) mma_commit(bar(C::B_SFULL));
             if (it + 2 == n && leader) mma_commit(bar(C::B_QEMPTY));
+            // dP(it+1) into the other block (its dS(it-1) was read by dQ(it-1))
+            const int nv = (gi + 1) % C::VST;
+            ok = wait(C::B_VFULL + nv, (gi + 1) / C::VST);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V + nv * C::TILE, C::dp_col((gi + 1) & 1));
+            if (leader) mma_commit(bar(C::B_DPFULL + ((gi + 1) & 1)));
+            if (leader) mma_commit(bar(C::B_VEMPTY + nv));
+            if (it + 2 == n && leader) mma_commit(bar(C::B_DOEMPTY));
           }
+          // dS(it) in TMEM; for the item's first tile this also means the
+          // softmax warps have stored the previous item's dQ
           ok = wait(C::B_PFULL, gi);
           if (!ok) break;
           tc_fence_after();
@@ -786,23 +796,12 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
           const uint64_t kdesc = make_sdesc(sbase + C::OFF_K + ks * C::TILE, C::REGION, 1024, 2);
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk)
-            if (leader) mma_ts(tmem + dq_col, tmem + C::ds_col(kk), kdesc + ((kk * 16 * 128) >> 4), idesc_q,
+            if (leader) mma_ts(tmem + C::DQ_COL, tmem + C::ds_col(gi & 1, kk), kdesc + ((kk * 16 * 128) >> 4), idesc_q,
                                (it > 0 || kk > 0) ? 1u : 0u);
           if (leader) mma_commit(bar(C::B_KEMPTY + ks));
-          if (more) {
-            // dP(it+1) overwrites the dS columns the MMAs above read (in order)
-            const int nv = (gi + 1) % C::VST;
-            ok = wait(C::B_VFULL + nv, (gi + 1) / C::VST);
-            if (!ok) break;
-            tc_fence_after();
-            if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V + nv * C::TILE, C::DP_COL);
-            if (leader) mma_commit(bar(C::B_DPFULL));
-            if (leader) mma_commit(bar(C::B_VEMPTY + nv));
-            if (it + 2 == n && leader) mma_commit(bar(C::B_DOEMPTY));
-          }
         }
         if (!ok) break;
-        if (leader) mma_commit(bar(C::B_DONE + buf));  // this item's dQ is final
+        if (leader) mma_commit(bar(C::B_DONE));  // this item's dQ is final
         gt += n;
         ++ln;
       }
@@ -818,7 +817,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint64_t c2 = f2_pack(s.scale_log2, s.scale_log2);
-    const uint32_t col = C::DP_COL + wg * C::CW;
+    const uint32_t col0 = C::DP_COL0 + wg * C::CW;  // this warpgroup's chunk of dP block 0
     using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
     // LSE and D of this thread's row of an item (loaded one item ahead)
     auto row_stats = [&](const DqItem& u, float* L, float* dv) {
@@ -861,9 +860,10 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
             sv[q] = (q >= lo && q < hi) ? sv[q] : __float_as_uint(-INFINITY);
         }
         exp2_scores32(sv, c2, nullptr, false, nl2x2);  // sv now holds P (fp32)
-        ok = mbar_wait(bar(C::B_DPFULL), gi & 1, tmo, abort_flag, wc.status);
+        ok = mbar_wait(bar(C::B_DPFULL + (gi & 1)), (gi >> 1) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t col = col0 + 128 * (gi & 1);
         uint32_t pv[32];
         tmem_ld32(tmem + lane_base + col, pv);
         tmem_ld_wait();
@@ -897,9 +897,8 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       // 16-column chunks of the dQ row dealt round-robin over the softmax
       // warpgroups; then the accumulator is free for the item after next
       const bool have = t.n_iter > 0;
-      const int buf = ln & 1;
       if (have) {
-        ok = mbar_wait(bar(C::B_DONE + buf), (ln >> 1) & 1, tmo, abort_flag, wc.status);
+        ok = mbar_wait(bar(C::B_DONE), ln & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         tc_fence_after();
       }
@@ -911,12 +910,10 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                      (static_cast<int64_t>(t.bh) * s.Tq + (rows_valid > 0 ? row0 : 0)) * C::D;
 #pragma unroll 1
       for (int task = wg; task < C::D / 32; task += C::NWG)
-        store_acc_block<4, C::BF16>(tmem + lane_base + C::DQ_COL + 128 * buf + task * 32, have, scale,
+        store_acc_block<4, C::BF16>(tmem + lane_base + C::DQ_COL + task * 32, have, scale,
                                     dst_blk + task * 32, C::D, rows_valid);
       if (have) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_ACCFREE + buf));
+        tc_fence_before();  // the next item's first dQ follows these reads
         gt += t.n_iter;
         ++ln;
       }
