@@ -11,7 +11,9 @@
 //
 // GB300 design (not the pages'): one CTA owns NQ query tiles of 128 rows of
 // one (batch, head). Roles per CTA:
-//   warp 0       TMA producer: Q tiles once, then K_j / V_j into a STAGES ring
+//   warps 0, 3   TMA producers: Q tiles once per block and the K ring
+//                (warp 0), the V ring (warp 3); a K slot frees when the last
+//                score MMA reading it completes, a V slot after the last PV
 //   warp 1       MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, then
 //                O_t += P_t V_j with P_t read straight from TMEM
 //   warp 2       TMEM allocator
@@ -77,10 +79,11 @@ struct FwdCfg {
   static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
   static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE;
-  // barriers: q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[NQ],
-  // p_full[NQ], o_ready[NQ], drain, item responses full[kClcSlots] / empty[kClcSlots]
+  // barriers: q_full, q_empty, k_full[S], v_full[S], k_empty[S], v_empty[S],
+  // s_full[NQ], p_full[NQ], o_ready[NQ], drain, item responses full / empty
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = B_KFULL + STAGES,
-                       B_KVEMPTY = B_VFULL + STAGES, B_SFULL = B_KVEMPTY + STAGES,
+                       B_KEMPTY = B_VFULL + STAGES, B_VEMPTY = B_KEMPTY + STAGES,
+                       B_SFULL = B_VEMPTY + STAGES,
                        B_PFULL = B_SFULL + NQ, B_OREADY = B_PFULL + NQ, B_DRAIN = B_OREADY + NQ,
                        B_CLCFULL = B_DRAIN + 1, B_CLCEMPTY = B_CLCFULL + kClcSlots,
                        NBAR = B_CLCEMPTY + kClcSlots;
@@ -88,7 +91,7 @@ struct FwdCfg {
   static constexpr int OFF_MISC = OFF_CLC + 16 * kClcSlots;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 128 + NQ * 128;
-  static constexpr int ITEM_WARPS = 2 + 4 * NQ;  // warps that walk the items: 0, 1, softmax
+  static constexpr int ITEM_WARPS = 3 + 4 * NQ;  // warps that walk the items: 0, 1, 3, softmax
   // Registers per thread after the split (0: no split): the producer / MMA
   // warpgroup hands registers to the softmax warpgroups, whose 128-score rows
   // would otherwise spill. The launch must hold THREADS x launch registers >=
@@ -126,7 +129,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     *abort_flag = 0;
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i >= C::B_PFULL && i < C::B_PFULL + C::NQ) cnt = 128;  // every softmax thread
+      if (i >= C::B_PFULL && i < C::B_PFULL + C::NQ) cnt = 4;  // one arrival per softmax warp
       if (i >= C::B_CLCEMPTY && i < C::B_CLCEMPTY + kClcSlots) cnt = C::ITEM_WARPS;
       mbar_init(bar(i), cnt);
     }
@@ -143,63 +146,65 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 
   if (warp < 4) {
   if constexpr (C::REG_CTRL > 0) regs_release<C::REG_CTRL>();
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Q of each block once its previous contents were last read, then the
-    // block's K_j / V_j into the ring (and the item requests). The whole warp
-    // runs the loop (a lone active lane whose siblings wait at the final
-    // barrier issues far slower); one elected lane issues.
+  if (warp == 0 || warp == 3) {
+    // ----------------------------------------------------------- producers
+    // warp 0: Q of each block (once its previous contents were last read),
+    // then the block's K ring tiles, and the item requests; warp 3: the V
+    // ring. The whole warp runs the loop (a lone active lane whose siblings
+    // wait at the final barrier issues far slower); one elected lane issues.
     const bool leader = elect_one_sync();
-    if (leader) tma_prefetch_desc(&map_q);
-    if (leader) tma_prefetch_desc(&map_k);
-    if (leader) tma_prefetch_desc(&map_v);
+    const bool k_ring = warp == 0;
+    if (leader) tma_prefetch_desc(k_ring ? &map_k : &map_v);
+    if (leader && k_ring) tma_prefetch_desc(&map_q);
     // K / V tiles are read by every query block of the group's heads: keep
     // them in L2; each Q block is read once
     const uint64_t pol_kv = l2_policy_evict_last(), pol_q = l2_policy_evict_first();
-    int gk = 0, ln = 0, asked = 0;  // ring tiles issued, blocks with work, requests
+    const int full = k_ring ? C::B_KFULL : C::B_VFULL, empty = k_ring ? C::B_KEMPTY : C::B_VEMPTY;
+    const uint32_t ring = sbase + (k_ring ? C::OFF_K : C::OFF_V);
+    const CUtensorMap* map = k_ring ? &map_k : &map_v;
+    int gk = 0, ln = 0, asked = 0;  // ring tiles issued, Q loads, requests
     bool ok = true;
     for (int k = 0, item = blockIdx.x; ok; ++k) {
-      ok = clc_request(iq, k, leader, tmo, abort_flag, wc.status);
-      if (!ok) break;
-      ++asked;
+      if (k_ring) {
+        ok = clc_request(iq, k, leader, tmo, abort_flag, wc.status);
+        if (!ok) break;
+        ++asked;
+      }
       const FwdItem t = fwd_item(item, order, s, ROWS, C::BN);
       if (t.n_iter > 0) {
-        if (ln > 0) ok = mbar_wait(bar(C::B_QEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
-        if (!ok) break;
-        if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL), C::NQ * C::Q_TILE);
-        for (int tq = 0; tq < C::NQ; ++tq)
-          for (int r = 0; r < C::KREG; ++r)
-            if (leader)
-              tma_load_3d_hint(sbase + C::OFF_Q + tq * C::Q_TILE + r * C::Q_REGION, &map_q, bar(C::B_QFULL),
-                               r * 64, t.q0 + tq * kBM, t.bh, pol_q);
-        ++ln;
+        if (k_ring) {
+          if (ln > 0) ok = mbar_wait(bar(C::B_QEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
+          if (!ok) break;
+          if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL), C::NQ * C::Q_TILE);
+          for (int tq = 0; tq < C::NQ; ++tq)
+            for (int r = 0; r < C::KREG; ++r)
+              if (leader)
+                tma_load_3d_hint(sbase + C::OFF_Q + tq * C::Q_TILE + r * C::Q_REGION, &map_q,
+                                 bar(C::B_QFULL), r * 64, t.q0 + tq * kBM, t.bh, pol_q);
+          ++ln;
+        }
         const int zkv = t.b * s.Hkv + t.g;
         for (int it = 0; it < t.n_iter; ++it, ++gk) {
           const int st = gk % C::STAGES;
           if (gk >= C::STAGES)
-            ok = mbar_wait(bar(C::B_KVEMPTY + st), ((gk / C::STAGES) - 1) & 1, tmo, abort_flag, wc.status);
+            ok = mbar_wait(bar(empty + st), ((gk / C::STAGES) - 1) & 1, tmo, abort_flag, wc.status);
           if (!ok) break;
-          const int krow = (t.j_lo + it) * C::BN;
-          if (leader) mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::KV_TILE);
+          if (leader) mbar_arrive_expect_tx(bar(full + st), C::KV_TILE);
           for (int r = 0; r < C::KREG; ++r)
             if (leader)
-              tma_load_3d_hint(sbase + C::OFF_K + st * C::KV_TILE + r * C::KV_REGION, &map_k,
-                               bar(C::B_KFULL + st), r * 64, krow, zkv, pol_kv);
-          if (leader) mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::KV_TILE);
-          for (int r = 0; r < C::KREG; ++r)
-            if (leader)
-              tma_load_3d_hint(sbase + C::OFF_V + st * C::KV_TILE + r * C::KV_REGION, &map_v,
-                               bar(C::B_VFULL + st), r * 64, krow, zkv, pol_kv);
+              tma_load_3d_hint(ring + st * C::KV_TILE + r * C::KV_REGION, map, bar(full + st), r * 64,
+                               (t.j_lo + it) * C::BN, zkv, pol_kv);
         }
         if (!ok) break;
       }
       if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
     }
     if (*abort_flag) {
-      drain_ring(bar(C::B_QFULL), 1, ln, tmo, wc.status);
-      drain_ring(bar(C::B_KFULL), C::STAGES, gk, tmo, wc.status);
-      drain_ring(bar(C::B_VFULL), C::STAGES, gk, tmo, wc.status);
-      drain_ring(iq.full, kClcSlots, asked, tmo, wc.status);
+      drain_ring(bar(full), C::STAGES, gk, tmo, wc.status);
+      if (k_ring) {
+        drain_ring(bar(C::B_QFULL), 1, ln, tmo, wc.status);
+        drain_ring(iq.full, kClcSlots, asked, tmo, wc.status);
+      }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
@@ -245,6 +250,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           if (leader) issue_s(tq, gk % C::STAGES);
           if (leader) mma_commit(bar(C::B_SFULL + tq));
         }
+        if (leader) mma_commit(bar(C::B_KEMPTY + gk % C::STAGES));  // K read for the last time
         if (n == 1 && leader) mma_commit(bar(C::B_QEMPTY));  // Q read for the last time
         for (int it = 0; it < n; ++it) {
           const int gi = gk + it;
@@ -271,7 +277,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           }
           if (!ok) break;
           if (it + 2 == n && leader) mma_commit(bar(C::B_QEMPTY));
-          if (leader) mma_commit(bar(C::B_KVEMPTY + st));
+          if (it + 1 < n && leader) mma_commit(bar(C::B_KEMPTY + nst));  // K(it+1) read by its last S
+          if (leader) mma_commit(bar(C::B_VEMPTY + st));                 // V(it) read by its last PV
         }
         if (!ok) break;
         gk += n;
@@ -377,7 +384,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(C::B_PFULL + tq));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_PFULL + tq));
       }
       if (!ok) break;
 
