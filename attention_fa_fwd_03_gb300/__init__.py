@@ -19,7 +19,8 @@ import threading
 
 __all__ = ["FA_FP16", "FA_BF16", "FaError", "fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkv",
            "fa_bwd_dq", "fa_bwd_workspace_size",
-           "fa_status_string", "fa_device_status", "fa_abi_version", "library", "library_path"]
+           "fa_status_string", "fa_device_status", "fa_abi_version", "fa_selftest_wait_timeout",
+           "library", "library_path"]
 
 FA_FP16 = 0
 FA_BF16 = 1
@@ -74,6 +75,8 @@ def library():
         lib.fa_device_status.restype = i
         lib.fa_abi_version.argtypes = []
         lib.fa_abi_version.restype = i
+        lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+        lib.fa_selftest_wait_timeout.restype = i
         _lib = lib
         return lib
 
@@ -190,6 +193,14 @@ def fa_bwd_dq(q, k, v, do, lse, workspace, dq, scale: float, causal: bool = Fals
                              _ptr(dq), B, Hq, Hkv, Tq, Tkv, D, float(scale), int(bool(causal)),
                              int(window), _dtype_code(q), _stream(stream))
     _check(st, "fa_bwd_dq")
+
+
+def fa_selftest_wait_timeout(timeout_ms: int, stream=None) -> None:
+    """Launch the library's bounded-wait self-test (see include/fa.h): a wait
+    that can never complete gives up after ``timeout_ms``; read the result
+    with fa_device_status()."""
+    _check(library().fa_selftest_wait_timeout(int(timeout_ms), _stream(stream)),
+           "fa_selftest_wait_timeout")
 
 
 def fa_device_status(clear: bool = True, stream=None) -> int:

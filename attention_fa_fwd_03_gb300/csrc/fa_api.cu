@@ -130,6 +130,43 @@ using namespace fa;
 
 extern "C" {
 
+}  // extern "C"
+
+namespace fa_selftest {
+
+// Two warps, two mbarriers that never complete (count 2, one arrival). Warp 0
+// waits with the given limit and gives up; warp 1 waits with four times that
+// limit and leaves through the abort flag warp 0 raised.
+__global__ void fa_selftest_wait_kernel(uint32_t* status, uint64_t cycles) {
+  __shared__ __align__(8) uint64_t never[2];
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    fa::mbar_init(fa::smem_u32(&never[0]), 2);
+    fa::mbar_init(fa::smem_u32(&never[1]), 2);
+    fa::fence_mbar_init();
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) fa::mbar_arrive(fa::smem_u32(&never[warp]));
+  __syncwarp();
+  fa::mbar_wait(fa::smem_u32(&never[warp]), 0, warp == 0 ? cycles : 4 * cycles, &abort_flag, status);
+  __syncthreads();
+}
+
+}  // namespace fa_selftest
+
+extern "C" {
+
+fa_status fa_selftest_wait_timeout(unsigned int timeout_ms, cudaStream_t stream) {
+  if (timeout_ms < 1 || timeout_ms > 10000) return FA_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  if (!status_ptr(&status)) return FA_ERR_LAUNCH;
+  const uint64_t cycles = static_cast<uint64_t>(timeout_ms) * 2200000ull;
+  fa_selftest::fa_selftest_wait_kernel<<<1, 64, 0, stream>>>(status, cycles);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 int fa_abi_version(void) { return 100; }
 
 const char* fa_status_string(fa_status s) {

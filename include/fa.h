@@ -161,6 +161,18 @@ const char* fa_status_string(fa_status s);
  * read itself failed. */
 fa_status fa_device_status(unsigned int* bits, int clear, cudaStream_t stream);
 
+/* Self-test of the bounded waits (a library check; the pages have no
+ * counterpart). Launches one small kernel on `stream` in which one warp waits
+ * on an mbarrier that can never complete, with a limit of `timeout_ms`
+ * milliseconds, and a second warp waits on another such barrier with four
+ * times that limit. The first wait gives up, sets FA_ERR_TIMEOUT's bit in the
+ * device status word and raises the kernel's abort flag, which lets the second
+ * warp leave at once; the kernel then exits normally and the context stays
+ * usable. Read the result with fa_device_status(). Returns FA_OK once the
+ * kernel is launched, FA_ERR_INVALID_ARG for timeout_ms outside 1..10000,
+ * FA_ERR_LAUNCH on a launch failure. */
+fa_status fa_selftest_wait_timeout(unsigned int timeout_ms, cudaStream_t stream);
+
 /* Version of this ABI (major * 100 + minor). */
 int fa_abi_version(void);
 
