@@ -232,8 +232,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           mma_ts(tmem + C::O_COL(tq), tmem + C::S_COL(tq) + kk * 8, bd, idesc_o, (acc || kk > 0) ? 1u : 0u);
       }
     };
+    // the issuer polls (test_wait), so it issues the moment a barrier completes
     auto wait = [&](int b, int parity) {
-      return mbar_wait(bar(b), parity & 1, tmo, abort_flag, wc.status);
+      return mbar_wait_poll(bar(b), parity & 1, tmo, abort_flag, wc.status);
     };
     int gk = 0, ln = 0;
     bool ok = true;
