@@ -579,12 +579,17 @@ struct DqCfg {
   static constexpr int OFF_V = OFF_K + KST * TILE;
   static constexpr int OFF_BAR = OFF_V + VST * TILE;
   // barriers: q_full, q_empty, do_full, do_empty, k_full[KST], k_empty[KST],
-  // v_full[VST], v_empty[VST], s_full, s_free, dp_full[2], p_full, done, drain
+  // v_full[VST], v_empty[VST], s_full, s_free, dp_full[2], p_full[2], done,
+  // drain. p_full alternates with the tile's parity: S and dP of tile j+1 are
+  // issued before the MMA waits for dS(j), so one softmax warp can finish
+  // tile j+1 while another still works on tile j; with a single barrier its
+  // second arrival would complete tile j's phase early. Two tiles ahead is
+  // impossible (S(j+2) waits for every warp's s_free of tile j+1).
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_DOFULL = 2, B_DOEMPTY = 3, B_KFULL = 4,
                        B_KEMPTY = B_KFULL + KST, B_VFULL = B_KEMPTY + KST,
                        B_VEMPTY = B_VFULL + VST, B_SFULL = B_VEMPTY + VST,
                        B_SFREE = B_SFULL + 1, B_DPFULL = B_SFULL + 2, B_PFULL = B_SFULL + 4,
-                       B_DONE = B_SFULL + 5, B_DRAIN = B_DONE + 1,
+                       B_DONE = B_SFULL + 6, B_DRAIN = B_DONE + 1,
                        B_CLCFULL = B_DRAIN + 1, B_CLCEMPTY = B_CLCFULL + kClcSlots,
                        NBAR = B_CLCEMPTY + kClcSlots;
   static constexpr int OFF_CLC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // item responses
@@ -635,7 +640,8 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     *abort_flag = 0;
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == C::B_PFULL || i == C::B_SFREE) cnt = 4 * C::NWG;  // one arrival per softmax warp
+      if (i == C::B_PFULL || i == C::B_PFULL + 1 || i == C::B_SFREE)
+        cnt = 4 * C::NWG;  // one arrival per softmax warp
       if (i >= C::B_CLCEMPTY && i < C::B_CLCEMPTY + kClcSlots) cnt = C::THREADS / 32;
       mbar_init(bar(i), cnt);
     }
@@ -789,7 +795,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
           }
           // dS(it) in TMEM; for the item's first tile this also means the
           // softmax warps have stored the previous item's dQ
-          ok = wait(C::B_PFULL, gi);
+          ok = wait(C::B_PFULL + (gi & 1), gi >> 1);
           if (!ok) break;
           tc_fence_after();
           // dQ += dS K   (dS from TMEM, K as MN-major B, K = key rows)
@@ -881,7 +887,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_PFULL));
+        if (lane == 0) mbar_arrive(bar(C::B_PFULL + (gi & 1)));
       }
       if (!ok) break;
       // the next item and its row statistics, loaded while this one is stored
