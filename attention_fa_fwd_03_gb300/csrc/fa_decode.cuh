@@ -1,0 +1,381 @@
+// Forward for short query blocks (at most 8 query rows per head): split over
+// the keys, on CUDA cores, one cluster of CTAs per (batch, query head).
+//
+// What it computes is the forward of page "mlx-bun 0.0.4: package/src/model/
+// flash-attention.ts" (forward shader): O = softmax(s Q K^T + mask) V with the
+// running max / running sum recurrence and the natural-log LSE per row, the
+// exp2 domain of page "[Metal] Add Flash Attention VJP for training"
+// (Implementation Notes). The page "[Metal] Add Flash Attention VJP for
+// training" also names a dedicated short-query (vector) path beside the tile
+// kernels; this is that path, designed for GB300.
+//
+// Why a separate kernel: with Tq <= 8 a 128-row tensor-core tile is at least
+// 94% padding, and the tile kernel walks all keys of a head in one CTA, so a
+// decode-shaped call is a serial chain of key tiles on a handful of SMs. Here
+// the keys of one (batch, head) are cut into `split` contiguous slices, one per
+// CTA of a thread-block cluster (split <= 8, the portable cluster size):
+//   - the slice is walked in stages of 128 keys: TMA copies the stage's K and
+//     V rows into shared memory (128-byte swizzle, double-buffered when it
+//     fits) while the previous stage is computed;
+//   - each warp takes 32 keys of a stage; a lane computes the scores of one
+//     key against the (pre-scaled) query rows held in shared memory, the warp
+//     keeps a running max / sum per row (online softmax, exp2 domain), and for
+//     P V a lane owns pairs of output columns (the swizzle keeps both the
+//     row-per-lane and the column-per-lane reads free of bank conflicts);
+//   - the CTA merges its warps' (max, sum, output) per row and stores the
+//     result straight into the shared memory of the row's owner, rank
+//     (row mod split), through distributed shared memory;
+//   - after one cluster barrier every owner merges its rows' partials from
+//     its own shared memory and writes O and LSE.
+// Waits: the stage loads complete on mbarriers with the library's bounded
+// wait (a wait that gives up sets the status word and the CTA skips the rest
+// of its keys); the cluster barriers (one at the start, split into arrive and
+// wait, so that no CTA writes into a peer that has not started, and one after
+// the partial rows are pushed) are reached by every thread of every CTA
+// unconditionally.
+// The merge is exact: each partial output is rescaled by 2^(m_part - m) to the
+// common max m before the sums, and a row no key is visible to gets O = 0 and
+// LSE = -inf.
+#pragma once
+
+#include "fa_common.cuh"
+
+namespace fa {
+
+constexpr int kDecodeMaxTq = 8;       // query rows per head the path takes
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeThreads = 32 * kDecodeWarps;
+constexpr int kDecodeMaxSplit = 8;    // CTAs per cluster (portable size)
+
+template <int D_, int TQ_, bool BF16_>
+struct DecodeFwdCfg {
+  static constexpr int D = D_;
+  static constexpr int TQ = TQ_;                  // query rows held (Tq rounded up to 1, 2, 4, 8)
+  static constexpr bool BF16 = BF16_;
+  static constexpr int NP = (D / 2 + 31) / 32;    // output column pairs per lane
+  static constexpr int SK = 32 * kDecodeWarps;    // keys per stage
+  static constexpr int DP = (D + 63) / 64 * 64;   // row padded to whole 128-byte column blocks
+  static constexpr int KREG = DP / 64;
+  static constexpr int REGION = SK * 128;         // bytes of one 64-column block of a stage
+  static constexpr int TILE = KREG * REGION;      // K (or V) rows of one stage
+  static constexpr int STAGES = D <= 128 ? 2 : 1;
+  // shared memory: stages first (1024-byte aligned), then floats
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + STAGES * TILE;
+  static constexpr int OFF_F = OFF_V + STAGES * TILE;
+  static constexpr int F_Q = 0;                                // [TQ][D] q * scale * log2(e)
+  static constexpr int F_P = F_Q + TQ * D;                     // [warps][TQ][32] p of a key block
+  static constexpr int F_OW = F_P + kDecodeWarps * TQ * 32;    // [warps][TQ][D] warp partial o
+  static constexpr int F_MW = F_OW + kDecodeWarps * TQ * D;    // [warps][TQ] warp max
+  static constexpr int F_LW = F_MW + kDecodeWarps * TQ;        // [warps][TQ] warp sum
+  // partial rows the cluster pushes to this CTA: slot (i / split) * split + rank
+  // of row i's owner (rank i % split) holds rank's o[D], max, sum
+  static constexpr int RSLOTS = TQ + kDecodeMaxSplit;
+  static constexpr int F_R = F_LW + kDecodeWarps * TQ;         // [RSLOTS][D + 2]
+  static constexpr int F_END = F_R + RSLOTS * (D + 2);
+  static constexpr int SMEM_BYTES = OFF_F + F_END * 4 + 1024;  // + alignment slack
+  static_assert(TQ >= 1 && TQ <= kDecodeMaxTq, "query rows");
+  static_assert(D % 8 == 0, "16-byte chunks");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+// Byte offset of element d of row r in a stage tile (64-column blocks of
+// 128-byte rows, 128-byte swizzle as TMA writes it).
+__device__ __forceinline__ uint32_t stage_offset(int region_bytes, int r, int d) {
+  return static_cast<uint32_t>((d >> 6) * region_bytes) +
+         sw128_offset(static_cast<uint32_t>(r), static_cast<uint32_t>((d & 63) >> 3)) +
+         static_cast<uint32_t>((d & 7) * 2);
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Split cluster barrier: every CTA of the cluster has started (its shared
+// memory may be written by peers) once the wait returns.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Every thread of every CTA of the cluster arrives; release / acquire order
+// the shared-memory writes before the barrier with the peers' reads after it.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store v to CTA `rank`'s shared memory, at the offset `p` has in this CTA's.
+__device__ __forceinline__ void st_peer_f32(float* p, uint32_t rank, float v) {
+  uint32_t remote, local = smem_u32(p);
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// 2^(x - m) with 2^(-inf) = 0 and no NaN when both are -inf.
+__device__ __forceinline__ float exp2_rel(float x, float m) {
+  return x == -INFINITY ? 0.f : exp2f(x - m);
+}
+
+// Grid: B * Hq clusters of `split` CTAs along x (CTA = cluster * split + rank).
+// Keys [k_first, k_last) are the ones any of the head's query rows can see;
+// CTA `rank` takes [k_first + rank * keys_per_cta, ...) of them. map_k / map_v
+// tile the [B * Hkv, Tkv, D] K and V with 64 x 128-row boxes.
+template <class C>
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+fa_fwd_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                     const uint16_t* __restrict__ q, uint16_t* __restrict__ o,
+                     float* __restrict__ lse, AttnShape s, int split, int k_first, int k_last,
+                     int keys_per_cta, WaitCfg wc) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[C::STAGES];
+  __shared__ int abort_flag;
+  constexpr int D = C::D, TQ = C::TQ;
+  // the swizzle pattern follows shared-memory address bits: align the stages to 1024 bytes
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  float* sm = reinterpret_cast<float*>(smem + C::OFF_F);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int bh = blockIdx.x / split;
+  const int b = bh / s.Hq;
+  const int g = (bh - b * s.Hq) / (s.Hq / s.Hkv);
+  const int zkv = b * s.Hkv + g;
+  const int Tq = s.Tq;
+  const int64_t q_row0 = static_cast<int64_t>(bh) * Tq;
+  const int kbeg = min(k_last, k_first + static_cast<int>(rank) * keys_per_cta);
+  const int kend = min(k_last, kbeg + keys_per_cta);
+  const int nstage = (kend - kbeg + C::SK - 1) / C::SK;
+  const uint64_t tmo = wc.timeout_cycles;
+  cluster_arrive_relaxed();  // waited for before the first store into a peer
+
+  // stage i: K and V rows [kbeg + i * SK, + SK) into slot i % STAGES
+  auto issue = [&](int i) {
+    const int slot = i % C::STAGES;
+    const uint32_t bar = smem_u32(&full[slot]);
+    mbar_arrive_expect_tx(bar, 2 * C::TILE);
+    for (int r = 0; r < C::KREG; ++r) {
+      tma_load_3d(sbase + C::OFF_K + slot * C::TILE + r * C::REGION, &map_k, bar, r * 64,
+                  kbeg + i * C::SK, zkv);
+      tma_load_3d(sbase + C::OFF_V + slot * C::TILE + r * C::REGION, &map_v, bar, r * 64,
+                  kbeg + i * C::SK, zkv);
+    }
+  };
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < C::STAGES; ++i) mbar_init(smem_u32(&full[i]), 1);
+    fence_mbar_init();
+    for (int i = 0; i < C::STAGES && i < nstage; ++i) issue(i);
+  }
+
+  // query rows, scaled into the exp2 domain; rows past Tq are zero
+  float* qs = sm + C::F_Q;
+  for (int e = threadIdx.x; e < TQ * D; e += kDecodeThreads) {
+    const int i = e / D;
+    float x = 0.f;
+    if (i < Tq) {
+      const uint32_t w = q[(q_row0 + i) * D + (e - i * D)];
+      x = unpack2<C::BF16>(w).x * s.scale_log2;
+    }
+    qs[e] = x;
+  }
+  __syncthreads();
+
+  float m[TQ], l[TQ], acc[TQ][C::NP][2];
+#pragma unroll
+  for (int i = 0; i < TQ; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+#pragma unroll
+    for (int u = 0; u < C::NP; ++u) acc[i][u][0] = acc[i][u][1] = 0.f;
+  }
+  float* ps = sm + C::F_P + warp * TQ * 32;
+
+  int done = 0;  // stages consumed
+#pragma unroll 1
+  for (int st = 0; st < nstage; ++st) {
+    const int slot = st % C::STAGES;
+    bool ok = mbar_wait(smem_u32(&full[slot]), (st / C::STAGES) & 1, tmo, &abort_flag, wc.status);
+    if (!__syncthreads_and(ok)) break;
+    done = st + 1;
+    const uint32_t ks = sbase + C::OFF_K + slot * C::TILE;
+    const uint32_t vs = sbase + C::OFF_V + slot * C::TILE;
+    const int blk = kbeg + st * C::SK + 32 * warp;  // this warp's 32 keys
+    if (blk < kend) {
+      const int rr = 32 * warp + lane;  // this lane's key row in the stage
+      const bool in = blk + lane < kend;
+      // scores of key blk + lane against every query row (lane = key)
+      float sc[TQ];
+#pragma unroll
+      for (int i = 0; i < TQ; ++i) sc[i] = 0.f;
+#pragma unroll 4
+      for (int c8 = 0; c8 < D / 8; ++c8) {
+        uint32_t w[4];
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(ks + stage_offset(C::REGION, rr, c8 * 8)));
+        float kf[8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 f = unpack2<C::BF16>(w[t]);
+          kf[2 * t] = f.x;
+          kf[2 * t + 1] = f.y;
+        }
+#pragma unroll
+        for (int i = 0; i < TQ; ++i) {
+          const float4 qa = *reinterpret_cast<const float4*>(qs + i * D + c8 * 8);
+          const float4 qb = *reinterpret_cast<const float4*>(qs + i * D + c8 * 8 + 4);
+          sc[i] = fmaf(qa.x, kf[0], sc[i]);
+          sc[i] = fmaf(qa.y, kf[1], sc[i]);
+          sc[i] = fmaf(qa.z, kf[2], sc[i]);
+          sc[i] = fmaf(qa.w, kf[3], sc[i]);
+          sc[i] = fmaf(qb.x, kf[4], sc[i]);
+          sc[i] = fmaf(qb.y, kf[5], sc[i]);
+          sc[i] = fmaf(qb.z, kf[6], sc[i]);
+          sc[i] = fmaf(qb.w, kf[7], sc[i]);
+        }
+      }
+      // mask, running max and sum, p of this block to shared memory
+#pragma unroll
+      for (int i = 0; i < TQ; ++i) {
+        int lo, hi;
+        visible_keys(s, i, blk, &lo, &hi);
+        if (!in || i >= Tq || lane < lo || lane >= hi) sc[i] = -INFINITY;
+        const float mn = fmaxf(m[i], warp_max(sc[i]));
+        const float alpha = exp2_rel(m[i], mn);
+        const float p = exp2_rel(sc[i], mn);
+        l[i] = l[i] * alpha + p;
+        m[i] = mn;
+#pragma unroll
+        for (int u = 0; u < C::NP; ++u) {
+          acc[i][u][0] *= alpha;
+          acc[i][u][1] *= alpha;
+        }
+        ps[i * 32 + lane] = p;
+      }
+      __syncwarp();
+      // o += p V over the block's keys (lane = output column pairs)
+      const int nj = min(32, kend - blk);
+#pragma unroll 4
+      for (int jj = 0; jj < nj; ++jj) {
+        float pj[TQ];
+#pragma unroll
+        for (int i = 0; i < TQ; ++i) pj[i] = ps[i * 32 + jj];
+#pragma unroll
+        for (int u = 0; u < C::NP; ++u) {
+          const int pidx = lane + 32 * u;
+          if (pidx < D / 2) {
+            uint32_t w;
+            asm volatile("ld.shared.u32 %0, [%1];"
+                         : "=r"(w)
+                         : "r"(vs + stage_offset(C::REGION, 32 * warp + jj, 2 * pidx)));
+            const float2 vf = unpack2<C::BF16>(w);
+#pragma unroll
+            for (int i = 0; i < TQ; ++i) {
+              acc[i][u][0] = fmaf(pj[i], vf.x, acc[i][u][0]);
+              acc[i][u][1] = fmaf(pj[i], vf.y, acc[i][u][1]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+    }
+    __syncthreads();  // every warp is done with this slot
+    if (threadIdx.x == 0 && st + C::STAGES < nstage) issue(st + C::STAGES);
+  }
+  // after a wait gave up: let the loads still in flight land before the CTA exits
+  if (threadIdx.x == 0)
+    for (int i = done; i < nstage && i < done + C::STAGES; ++i)
+      mbar_wait(smem_u32(&full[i % C::STAGES]), (i / C::STAGES) & 1, tmo, nullptr, wc.status);
+
+  // warp partials to shared memory
+  float* ow = sm + C::F_OW + warp * TQ * D;
+#pragma unroll
+  for (int i = 0; i < TQ; ++i) {
+    const float lsum = warp_sum(l[i]);
+    if (lane == 0) {
+      sm[C::F_MW + warp * TQ + i] = m[i];
+      sm[C::F_LW + warp * TQ + i] = lsum;
+    }
+#pragma unroll
+    for (int u = 0; u < C::NP; ++u) {
+      const int pidx = lane + 32 * u;
+      if (pidx < D / 2) {
+        ow[i * D + 2 * pidx] = acc[i][u][0];
+        ow[i * D + 2 * pidx + 1] = acc[i][u][1];
+      }
+    }
+  }
+  __syncthreads();
+  // CTA partial of each row (the warps' rows rescaled to their common max),
+  // pushed into the shared memory of the row's owner
+  float* recv = sm + C::F_R;
+  cluster_wait();  // every CTA of the cluster is running
+  for (int e = threadIdx.x; e < Tq * D; e += kDecodeThreads) {
+    const int i = e / D;
+    float mc = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) mc = fmaxf(mc, sm[C::F_MW + w * TQ + i]);
+    float x = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w)
+      x += sm[C::F_OW + w * TQ * D + e] * exp2_rel(sm[C::F_MW + w * TQ + i], mc);
+    const int slot = (i / split) * split + static_cast<int>(rank);
+    st_peer_f32(recv + slot * (D + 2) + (e - i * D), static_cast<uint32_t>(i % split), x);
+  }
+  if (threadIdx.x < Tq) {
+    const int i = threadIdx.x;
+    float mc = -INFINITY;
+    for (int w = 0; w < kDecodeWarps; ++w) mc = fmaxf(mc, sm[C::F_MW + w * TQ + i]);
+    float lc = 0.f;
+    for (int w = 0; w < kDecodeWarps; ++w)
+      lc += sm[C::F_LW + w * TQ + i] * exp2_rel(sm[C::F_MW + w * TQ + i], mc);
+    const int slot = (i / split) * split + static_cast<int>(rank);
+    st_peer_f32(recv + slot * (D + 2) + D, static_cast<uint32_t>(i % split), mc);
+    st_peer_f32(recv + slot * (D + 2) + D + 1, static_cast<uint32_t>(i % split), lc);
+  }
+  // every partial row has landed in its owner's shared memory; after this no
+  // CTA touches another's, so no second barrier is needed before exiting
+  cluster_barrier();
+
+  // this CTA owns query rows rank, rank + split, ...: merge the cluster's partials
+  using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
+  for (int i = static_cast<int>(rank); i < Tq; i += split) {
+    const float* rows = recv + (i / split) * split * (D + 2);  // split slots of D + 2
+    float mt = -INFINITY;
+    for (int c = 0; c < split; ++c) mt = fmaxf(mt, rows[c * (D + 2) + D]);
+    float lt = 0.f;
+    for (int c = 0; c < split; ++c)
+      lt += rows[c * (D + 2) + D + 1] * exp2_rel(rows[c * (D + 2) + D], mt);
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    T16* orow = reinterpret_cast<T16*>(o) + (q_row0 + i) * D;
+    for (int d = threadIdx.x; d < D; d += kDecodeThreads) {
+      float x = 0.f;
+      for (int c = 0; c < split; ++c)
+        x += rows[c * (D + 2) + d] * exp2_rel(rows[c * (D + 2) + D], mt);
+      if constexpr (C::BF16)
+        orow[d] = __float2bfloat16_rn(x * inv);
+      else
+        orow[d] = __float2half_rn(x * inv);
+    }
+    if (threadIdx.x == 0) lse[q_row0 + i] = lt > 0.f ? (mt + __log2f(lt)) * kLn2 : -INFINITY;
+  }
+}
+
+}  // namespace fa

@@ -3,10 +3,12 @@
 // stream. Each fa_inst_d*.cu picks the tile configuration for its head dim.
 #pragma once
 
+#include <algorithm>
 #include <type_traits>
 
 #include "fa_bwd.cuh"
 #include "fa_bwd_pipelined.cuh"
+#include "fa_decode.cuh"
 #include "fa_fwd.cuh"
 #include "fa_launch.h"
 
@@ -183,6 +185,57 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
   return e;
 }
 
+// Short query blocks (Tq <= 8): the split-key kernel of fa_decode.cuh. The
+// keys any query row can see are cut into `split` slices of whole 32-key
+// blocks, one per CTA of a cluster; split grows with the keys (128 per CTA at
+// least) until about two CTAs per SM are in flight, at most 8.
+template <class C>
+cudaError_t launch_fwd_decode(const FwdLaunch& a) {
+  int k_first, k_last;
+  key_range(a.s, 0, a.s.Tq, &k_first, &k_last);
+  const int nk = k_last - k_first;
+  const int64_t units = static_cast<int64_t>(a.s.B) * a.s.Hq;
+  const int64_t want_ctas = 2 * static_cast<int64_t>(device_sm_count());
+  int split = static_cast<int>((want_ctas + units - 1) / units);
+  split = std::min(split, std::max(1, (nk + 127) / 128));
+  split = std::max(1, std::min(split, kDecodeMaxSplit));
+  int per = (nk + split - 1) / split;
+  per = std::max(32, (per + 31) / 32 * 32);
+  split = std::max(1, (nk + per - 1) / per);
+  CUtensorMap mk, mv;
+  const int bhkv = a.s.B * a.s.Hkv;
+  if (!encode_tile_map(&mk, a.k, C::BF16, C::D, a.s.Tkv, bhkv, C::SK) ||
+      !encode_tile_map(&mv, a.v, C::BF16, C::D, a.s.Tkv, bhkv, C::SK))
+    return cudaErrorInvalidValue;
+  auto kern = fa_fwd_decode_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units * split), 1, 1);
+  cfg.blockDim = dim3(kDecodeThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mk, mv, static_cast<const uint16_t*>(a.q),
+                            static_cast<uint16_t*>(a.o), a.lse, a.s, split, k_first, k_last, per,
+                            a.wc);
+}
+
+template <int D, bool BF16>
+cudaError_t run_fwd_decode(const FwdLaunch& a) {
+  if (a.s.Tq <= 1) return launch_fwd_decode<DecodeFwdCfg<D, 1, BF16>>(a);
+  if (a.s.Tq <= 2) return launch_fwd_decode<DecodeFwdCfg<D, 2, BF16>>(a);
+  if (a.s.Tq <= 4) return launch_fwd_decode<DecodeFwdCfg<D, 4, BF16>>(a);
+  return launch_fwd_decode<DecodeFwdCfg<D, 8, BF16>>(a);
+}
+
 }  // namespace fa
 
 // Define launch_fwd_d<D> / launch_bwd_d<D> for one head dim, given the forward
@@ -191,6 +244,8 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
 #define FA_DEFINE_HEAD_DIM(D, FNQ, FBN, FST)                                              \
   namespace fa {                                                                          \
   cudaError_t launch_fwd_d##D(const FwdLaunch& a) {                                       \
+    if (a.s.Tq <= kDecodeMaxTq)                                                           \
+      return a.bf16 ? run_fwd_decode<D, true>(a) : run_fwd_decode<D, false>(a);           \
     return a.bf16 ? run_fwd<FwdCfg<D, FNQ, FBN, FST, true>>(a)                            \
                   : run_fwd<FwdCfg<D, FNQ, FBN, FST, false>>(a);                          \
   }                                                                                       \
