@@ -15,8 +15,8 @@
 // the keys of one (batch, head) are cut into `split` contiguous slices, one per
 // CTA of a thread-block cluster (split <= 8, the portable cluster size):
 //   - the slice is walked in stages of 128 keys: TMA copies the stage's K and
-//     V rows into shared memory (128-byte swizzle, double-buffered when it
-//     fits) while the previous stage is computed;
+//     V rows into shared memory (128-byte swizzle); the next stage is loaded
+//     once every warp is done with the current one;
 //   - each warp takes 32 keys of a stage; a lane computes the scores of one
 //     key against the (pre-scaled) query rows held in shared memory, the warp
 //     keeps a running max / sum per row (online softmax, exp2 domain), and for
@@ -58,7 +58,9 @@ struct DecodeFwdCfg {
   static constexpr int KREG = DP / 64;
   static constexpr int REGION = SK * 128;         // bytes of one 64-column block of a stage
   static constexpr int TILE = KREG * REGION;      // K (or V) rows of one stage
-  static constexpr int STAGES = D <= 128 ? 2 : 1;
+  // one stage: at D <= 128 two CTAs then fit on an SM, which doubles the warps
+  // that hide each other's latency and lets twice as many clusters run at once
+  static constexpr int STAGES = 1;
   // shared memory: stages first (1024-byte aligned), then floats
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + STAGES * TILE;
@@ -71,7 +73,8 @@ struct DecodeFwdCfg {
   // partial rows the cluster pushes to this CTA: slot (i / split) * split + rank
   // of row i's owner (rank i % split) holds rank's o[D], max, sum
   static constexpr int RSLOTS = TQ + kDecodeMaxSplit;
-  static constexpr int F_R = F_LW + kDecodeWarps * TQ;         // [RSLOTS][D + 2]
+  static constexpr int F_WT = F_LW + kDecodeWarps * TQ;        // [warps][TQ] 2^(warp max - CTA max)
+  static constexpr int F_R = F_WT + kDecodeWarps * TQ;         // [RSLOTS][D + 2]
   static constexpr int F_END = F_R + RSLOTS * (D + 2);
   static constexpr int SMEM_BYTES = OFF_F + F_END * 4 + 1024;  // + alignment slack
   static_assert(TQ >= 1 && TQ <= kDecodeMaxTq, "query rows");
@@ -326,29 +329,35 @@ fa_fwd_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_con
   // CTA partial of each row (the warps' rows rescaled to their common max),
   // pushed into the shared memory of the row's owner
   float* recv = sm + C::F_R;
-  cluster_wait();  // every CTA of the cluster is running
-  for (int e = threadIdx.x; e < Tq * D; e += kDecodeThreads) {
-    const int i = e / D;
-    float mc = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) mc = fmaxf(mc, sm[C::F_MW + w * TQ + i]);
-    float x = 0.f;
-#pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w)
-      x += sm[C::F_OW + w * TQ * D + e] * exp2_rel(sm[C::F_MW + w * TQ + i], mc);
-    const int slot = (i / split) * split + static_cast<int>(rank);
-    st_peer_f32(recv + slot * (D + 2) + (e - i * D), static_cast<uint32_t>(i % split), x);
-  }
   if (threadIdx.x < Tq) {
     const int i = threadIdx.x;
     float mc = -INFINITY;
     for (int w = 0; w < kDecodeWarps; ++w) mc = fmaxf(mc, sm[C::F_MW + w * TQ + i]);
     float lc = 0.f;
+    for (int w = 0; w < kDecodeWarps; ++w) {
+      const float wt = exp2_rel(sm[C::F_MW + w * TQ + i], mc);
+      sm[C::F_WT + w * TQ + i] = wt;
+      lc += sm[C::F_LW + w * TQ + i] * wt;
+    }
+    sm[C::F_MW + i] = mc;  // warp 0's max is no longer needed
+    sm[C::F_LW + i] = lc;
+  }
+  __syncthreads();
+  cluster_wait();  // every CTA of the cluster is running
+  for (int e = threadIdx.x; e < Tq * D; e += kDecodeThreads) {
+    const int i = e / D;
+    float x = 0.f;
+#pragma unroll
     for (int w = 0; w < kDecodeWarps; ++w)
-      lc += sm[C::F_LW + w * TQ + i] * exp2_rel(sm[C::F_MW + w * TQ + i], mc);
+      x += sm[C::F_OW + w * TQ * D + e] * sm[C::F_WT + w * TQ + i];
     const int slot = (i / split) * split + static_cast<int>(rank);
-    st_peer_f32(recv + slot * (D + 2) + D, static_cast<uint32_t>(i % split), mc);
-    st_peer_f32(recv + slot * (D + 2) + D + 1, static_cast<uint32_t>(i % split), lc);
+    st_peer_f32(recv + slot * (D + 2) + (e - i * D), static_cast<uint32_t>(i % split), x);
+  }
+  if (threadIdx.x < Tq) {
+    const int i = threadIdx.x;
+    const int slot = (i / split) * split + static_cast<int>(rank);
+    st_peer_f32(recv + slot * (D + 2) + D, static_cast<uint32_t>(i % split), sm[C::F_MW + i]);
+    st_peer_f32(recv + slot * (D + 2) + D + 1, static_cast<uint32_t>(i % split), sm[C::F_LW + i]);
   }
   // every partial row has landed in its owner's shared memory; after this no
   // CTA touches another's, so no second barrier is needed before exiting

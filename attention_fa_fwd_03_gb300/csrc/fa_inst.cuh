@@ -185,44 +185,69 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
   return e;
 }
 
-// Short query blocks (Tq <= 8): the split-key kernel of fa_decode.cuh. The
-// keys any query row can see are cut into `split` slices of whole 32-key
-// blocks, one per CTA of a cluster; split grows with the keys (128 per CTA at
-// least) until about two CTAs per SM are in flight, at most 8.
+// Short query blocks (Tq <= 8): the split-key kernel of fa_decode.cuh, one
+// cluster of `split` CTAs per (batch, query head). The cluster size trades the
+// keys each CTA walks (nk / split) against the waves the clusters need: the
+// device runs at most M(split) such clusters at once (queried once per kernel
+// and size), so the estimated time is ceil(clusters / M(split)) * nk / split.
+// Slices are whole 32-key blocks; a cluster never has more CTAs than 32-key
+// blocks to give them.
 template <class C>
 cudaError_t launch_fwd_decode(const FwdLaunch& a) {
   int k_first, k_last;
   key_range(a.s, 0, a.s.Tq, &k_first, &k_last);
   const int nk = k_last - k_first;
   const int64_t units = static_cast<int64_t>(a.s.B) * a.s.Hq;
-  const int64_t want_ctas = 2 * static_cast<int64_t>(device_sm_count());
-  int split = static_cast<int>((want_ctas + units - 1) / units);
-  split = std::min(split, std::max(1, (nk + 127) / 128));
-  split = std::max(1, std::min(split, kDecodeMaxSplit));
-  int per = (nk + split - 1) / split;
-  per = std::max(32, (per + 31) / 32 * 32);
-  split = std::max(1, (nk + per - 1) / per);
+  auto kern = fa_fwd_decode_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   CUtensorMap mk, mv;
   const int bhkv = a.s.B * a.s.Hkv;
   if (!encode_tile_map(&mk, a.k, C::BF16, C::D, a.s.Tkv, bhkv, C::SK) ||
       !encode_tile_map(&mv, a.v, C::BF16, C::D, a.s.Tkv, bhkv, C::SK))
     return cudaErrorInvalidValue;
-  auto kern = fa_fwd_decode_kernel<C>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units * split), 1, 1);
   cfg.blockDim = dim3(kDecodeThreads, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = a.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(split);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // clusters of each size the device holds at once (per device, cached)
+  static int max_active[64][kDecodeMaxSplit + 1] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int blocks32 = std::max(1, (nk + 31) / 32);
+  int split = 1;
+  double best = 0.0;
+  for (int sz = 1; sz <= kDecodeMaxSplit; sz *= 2) {
+    if (sz > 1 && sz > blocks32) break;
+    int m = dev >= 0 && dev < 64 ? max_active[dev][sz] : 0;
+    if (m == 0) {
+      cfg.gridDim = dim3(static_cast<unsigned>(sz), 1, 1);
+      attr[0].val.clusterDim.x = static_cast<unsigned>(sz);
+      if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess || m < 1) {
+        cudaGetLastError();  // clear; this size is not used
+        continue;
+      }
+      if (dev >= 0 && dev < 64) max_active[dev][sz] = m;
+    }
+    const double waves = static_cast<double>((units + m - 1) / m);
+    const double cost = waves * ((nk + sz - 1) / sz + 64);  // + per-CTA fixed work, in keys
+    if (sz == 1 || cost < best) {
+      best = cost;
+      split = sz;
+    }
+  }
+  int per = (nk + split - 1) / split;
+  per = std::max(32, (per + 31) / 32 * 32);
+  split = std::max(1, (nk + per - 1) / per);
+  cfg.gridDim = dim3(static_cast<unsigned>(units * split), 1, 1);
+  attr[0].val.clusterDim.x = static_cast<unsigned>(split);
   return cudaLaunchKernelEx(&cfg, kern, mk, mv, static_cast<const uint16_t*>(a.q),
                             static_cast<uint16_t*>(a.o), a.lse, a.s, split, k_first, k_last, per,
                             a.wc);
