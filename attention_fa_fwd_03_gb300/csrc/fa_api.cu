@@ -85,6 +85,20 @@ fa_status check_common(int B, int Hq, int Hkv, int Tq, int Tkv, int D, float sca
   return FA_OK;
 }
 
+// Mask-free attention with grouped query heads: the Tq rows of the r query
+// heads of one KV group are consecutive in memory ([B, Hq, Tq, D] is
+// [B, Hkv, r * Tq, D], and the LSE and D-vector [B, Hq, Tq] likewise), and
+// without a mask every row sees the same keys, so the call is the same
+// problem with Hq' = Hkv and Tq' = r * Tq. Below one 128-row tile this packs
+// the heads' rows into shared tiles instead of padding each head's few rows
+// to a tile of its own (and the dK/dV kernel then walks one query tile per
+// key tile instead of r). Rows with Tq <= min_tq are left alone.
+void fold_group_rows(int causal, int window, int Hkv, int min_tq, int* Hq, int* Tq) {
+  if (causal || window > 0 || *Hq == Hkv || *Tq >= kBM || *Tq <= min_tq) return;
+  *Tq *= *Hq / Hkv;
+  *Hq = Hkv;
+}
+
 AttnShape make_shape(int B, int Hq, int Hkv, int Tq, int Tkv, int causal, int window,
                      float scale) {
   AttnShape s;
@@ -205,7 +219,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     return FA_ERR_INVALID_ARG;
   FwdLaunch a;
   a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
-  a.s = make_shape(B, Hq, Hkv, Tq, Tkv, causal, window, scale);
+  int hq = Hq, tq = Tq;  // short query blocks keep the split-key kernel
+  fold_group_rows(causal, window, Hkv, kDecodeMaxTq, &hq, &tq);
+  a.s = make_shape(B, hq, Hkv, tq, Tkv, causal, window, scale);
   a.bf16 = dt == FA_BF16;
   if (!status_ptr(&a.wc.status)) return FA_ERR_LAUNCH;
   a.wc.timeout_cycles = wait_timeout_cycles();
@@ -264,7 +280,9 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   a.dq = dq; a.dk = dk; a.dv = dv;
   a.dvec = static_cast<float*>(dvec);
   a.scale = scale;
-  a.s = make_shape(B, Hq, Hkv, Tq, Tkv, causal, window, scale);
+  int hq = Hq, tq = Tq;
+  fold_group_rows(causal, window, Hkv, 0, &hq, &tq);
+  a.s = make_shape(B, hq, Hkv, tq, Tkv, causal, window, scale);
   a.bf16 = dt == FA_BF16;
   if (!status_ptr(&a.wc.status)) return FA_ERR_LAUNCH;
   a.wc.timeout_cycles = wait_timeout_cycles();

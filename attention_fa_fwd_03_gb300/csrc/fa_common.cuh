@@ -20,6 +20,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Rows of the query tile one MMA covers (M of tcgen05.mma, one TMEM lane each).
 constexpr int kBM = 128;
 
+// Forward calls with at most this many query rows per head take the
+// split-key CUDA-core kernel (fa_decode.cuh) instead of the tile kernel.
+constexpr int kDecodeMaxTq = 8;
+
 struct AttnShape {
   int B, Hq, Hkv, Tq, Tkv;
   int causal, window;

@@ -42,7 +42,6 @@
 
 namespace fa {
 
-constexpr int kDecodeMaxTq = 8;       // query rows per head the path takes
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeThreads = 32 * kDecodeWarps;
 constexpr int kDecodeMaxSplit = 8;    // CTAs per cluster (portable size)
