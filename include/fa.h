@@ -77,6 +77,10 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
  *   o [B,Hq,Tq,D]                      output, dtype `dt`
  *   lse [B,Hq,Tq]                      output, fp32 natural-log LSE (kept for fa_bwd)
  * Sizes: B, Hq, Hkv, Tq, Tkv >= 1; Tq, Tkv <= 2^22; B * Hq <= 2^24.
+ * One kernel launch. Tq <= 8 (decode-shaped calls) runs a split-key kernel
+ * that launches thread-block clusters of up to 8 CTAs; longer query blocks run
+ * the tensor-core tile kernel. Both compute the same result; which one runs
+ * changes only the rounding of the fp32 sums.
  * Returns FA_OK or an error code (nothing launched on error). */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int Hq, int Hkv, int Tq, int Tkv, int D, float scale,
