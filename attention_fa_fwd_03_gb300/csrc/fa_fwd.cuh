@@ -21,8 +21,12 @@
 //                writes P_t (16-bit) over its own S_t columns, rescales O_t
 //                in TMEM when the running max grows by more than 2^8, and
 //                finally normalises O_t and writes O and LSE.
-// With NQ = 2 the two softmax warpgroups ping-pong: while one computes its
-// softmax the tensor core works on the other tile's MMAs.
+// With NQ = 2 the two softmax warpgroups run side by side: while one computes
+// its softmax the tensor core works on the other tile's MMAs. Where TMEM has
+// room (one query tile with 64-key tiles, as at D = 256), each query tile has
+// two score buffers: S(j+1) is computed while the softmax turns S(j) into P(j),
+// so the softmax of consecutive tiles is not serialised behind PV(j) and the
+// next S (a single buffer, which P aliases, must wait for PV(j) to read P).
 // Persistent: a CTA that finishes its block takes over the next
 // not-yet-started CTA's block through cluster launch control (ItemQueue), so
 // one CTA per SM walks a balanced stream of blocks in launch order. The K/V
@@ -79,14 +83,25 @@ struct FwdCfg {
   static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
   static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE;
+  // Score buffers per query tile: two when they fit in TMEM next to the O
+  // accumulators. With two, S(j+1) is computed while the softmax works on
+  // S(j) (P(j) is written over S(j) and read by PV(j); S(j+2) reuses the
+  // buffer after PV(j) in issue order), so the softmax never waits for the
+  // tensor core to finish PV before its next scores exist.
+  static constexpr int SBUF = NQ * (2 * BN + DP) <= 512 ? 2 : 1;
   // barriers: q_full, q_empty, k_full[S], v_full[S], k_empty[S], v_empty[S],
-  // s_full[NQ], p_full[NQ], o_ready[NQ], drain, item responses full / empty
+  // s_full[NQ][SBUF], p_full[NQ][SBUF], o_ready[NQ], drain, item responses
+  // full / empty. p_full has one barrier per score buffer: with two buffers a
+  // softmax warp can finish tile j+1 while a sibling still works on tile j,
+  // and its arrival must not count towards tile j.
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = B_KFULL + STAGES,
                        B_KEMPTY = B_VFULL + STAGES, B_VEMPTY = B_KEMPTY + STAGES,
-                       B_SFULL = B_VEMPTY + STAGES,
-                       B_PFULL = B_SFULL + NQ, B_OREADY = B_PFULL + NQ, B_DRAIN = B_OREADY + NQ,
+                       B_SFULL = B_VEMPTY + STAGES, B_PFULL = B_SFULL + NQ * SBUF,
+                       B_OREADY = B_PFULL + NQ * SBUF, B_DRAIN = B_OREADY + NQ,
                        B_CLCFULL = B_DRAIN + 1, B_CLCEMPTY = B_CLCFULL + kClcSlots,
                        NBAR = B_CLCEMPTY + kClcSlots;
+  static constexpr int sfull(int t, int b) { return B_SFULL + t * SBUF + b; }
+  static constexpr int pfull(int t, int b) { return B_PFULL + t * SBUF + b; }
   static constexpr int OFF_CLC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;
   static constexpr int OFF_MISC = OFF_CLC + 16 * kClcSlots;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -96,13 +111,15 @@ struct FwdCfg {
   // warpgroup hands registers to the softmax warpgroups, whose 128-score rows
   // would otherwise spill. The launch must hold THREADS x launch registers >=
   // REG_NEEDED (checked on the host against the compiled kernel).
-  static constexpr int REG_CTRL = NQ == 2 ? 80 : 0, REG_SOFT = NQ == 2 ? 200 : 0;
+  static constexpr int REG_CTRL = NQ == 2 ? (SBUF == 2 ? 112 : 80) : 0,
+                       REG_SOFT = NQ == 2 ? (SBUF == 2 ? 168 : 200) : 0;
   static constexpr int REG_NEEDED = 128 * REG_CTRL + 128 * NQ * REG_SOFT;
-  static constexpr int S_COL(int t) { return t * 128; }
-  static constexpr int O_COL(int t) { return 256 + t * 128; }
+  // TMEM: score buffers of tile t at t * SBUF * BN + b * BN, O_t after all of them
+  static constexpr int S_COL(int t, int b) { return (t * SBUF + b) * BN; }
+  static constexpr int O_COL(int t) { return NQ * SBUF * BN + t * DP; }
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(BN % 32 == 0 && BN <= 128, "key tile");
-  static_assert(NQ * 128 <= 256 && (NQ == 1 || D <= 128), "TMEM budget");
+  static_assert(NQ * (SBUF * BN + DP) <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -129,7 +146,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     *abort_flag = 0;
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i >= C::B_PFULL && i < C::B_PFULL + C::NQ) cnt = 4;  // one arrival per softmax warp
+      if (i >= C::B_PFULL && i < C::B_PFULL + C::NQ * C::SBUF) cnt = 4;  // one per softmax warp
       if (i >= C::B_CLCEMPTY && i < C::B_CLCEMPTY + kClcSlots) cnt = C::ITEM_WARPS;
       mbar_init(bar(i), cnt);
     }
@@ -212,7 +229,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const bool leader = elect_one_sync();
     constexpr uint32_t idesc_s = make_idesc_f16(kBM, C::BN, C::BF16 ? 1 : 0, 0, 0);
     constexpr uint32_t idesc_o = make_idesc_f16(kBM, C::D, C::BF16 ? 1 : 0, 0, 1);
-    auto issue_s = [&](int tq, int st) {
+    // S of query tile tq against the K tile in ring slot st, into score buffer b
+    auto issue_s = [&](int tq, int st, int b) {
       const uint32_t qa = sbase + C::OFF_Q + tq * C::Q_TILE;
       const uint32_t ka = sbase + C::OFF_K + st * C::KV_TILE;
 #pragma unroll
@@ -220,16 +238,18 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const uint32_t off = (kk & 3) * 32;  // 16 elements = 32 bytes along K
         const uint64_t ad = make_sdesc(qa + (kk >> 2) * C::Q_REGION + off, 16, 1024, 2);
         const uint64_t bd = make_sdesc(ka + (kk >> 2) * C::KV_REGION + off, 16, 1024, 2);
-        if (leader) mma_ss(tmem + C::S_COL(tq), ad, bd, idesc_s, kk > 0);
+        if (leader) mma_ss(tmem + C::S_COL(tq, b), ad, bd, idesc_s, kk > 0);
       }
     };
-    auto issue_pv = [&](int tq, int st, bool acc) {
+    // O_tq += P V with P read from score buffer b
+    auto issue_pv = [&](int tq, int st, int b, bool acc) {
       const uint32_t va = sbase + C::OFF_V + st * C::KV_TILE;
 #pragma unroll
       for (int kk = 0; kk < C::BN / 16; ++kk) {
         const uint64_t bd = make_sdesc(va + kk * 16 * 128, C::KV_REGION, 1024, 2);
         if (leader)
-          mma_ts(tmem + C::O_COL(tq), tmem + C::S_COL(tq) + kk * 8, bd, idesc_o, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::O_COL(tq), tmem + C::S_COL(tq, b) + kk * 8, bd, idesc_o,
+                 (acc || kk > 0) ? 1u : 0u);
       }
     };
     // the issuer polls (test_wait), so it issues the moment a barrier completes
@@ -242,44 +262,52 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       const FwdItem t = fwd_item(item, order, s, ROWS, C::BN);
       const int n = t.n_iter;
       if (n > 0) {
-        // scores of the block's first key tile (over the P columns of the
-        // previous block, whose PV MMAs precede them in issue order)
-        ok = wait(C::B_QFULL, ln) && wait(C::B_KFULL + gk % C::STAGES, gk / C::STAGES);
-        if (!ok) break;
-        tc_fence_after();
-        for (int tq = 0; tq < C::NQ; ++tq) {
-          if (leader) issue_s(tq, gk % C::STAGES);
-          if (leader) mma_commit(bar(C::B_SFULL + tq));
+        // scores of the block's first SBUF key tiles (over score buffers whose
+        // PV MMAs of the previous block precede them in issue order)
+        ok = wait(C::B_QFULL, ln);
+        const int npro = n < C::SBUF ? n : C::SBUF;
+        for (int p = 0; p < npro && ok; ++p) {
+          const int gp = gk + p;
+          ok = wait(C::B_KFULL + gp % C::STAGES, gp / C::STAGES);
+          if (!ok) break;
+          tc_fence_after();
+          for (int tq = 0; tq < C::NQ; ++tq) {
+            if (leader) issue_s(tq, gp % C::STAGES, gp % C::SBUF);
+            if (leader) mma_commit(bar(C::sfull(tq, gp % C::SBUF)));
+          }
+          if (leader) mma_commit(bar(C::B_KEMPTY + gp % C::STAGES));  // K read for the last time
+          if (p == n - 1 && leader) mma_commit(bar(C::B_QEMPTY));    // Q read for the last time
         }
-        if (leader) mma_commit(bar(C::B_KEMPTY + gk % C::STAGES));  // K read for the last time
-        if (n == 1 && leader) mma_commit(bar(C::B_QEMPTY));  // Q read for the last time
+        if (!ok) break;
         for (int it = 0; it < n; ++it) {
           const int gi = gk + it;
-          const int st = gi % C::STAGES, nst = (gi + 1) % C::STAGES;
+          const int st = gi % C::STAGES, b = gi % C::SBUF;
+          const int gn = gi + C::SBUF, nst = gn % C::STAGES;  // the tile whose S reuses buffer b
+          const bool next = it + C::SBUF < n;
           ok = wait(C::B_VFULL + st, gi / C::STAGES);
           if (!ok) break;
           for (int tq = 0; tq < C::NQ; ++tq) {
             // P_t in TMEM; for the block's first tile this also means the
             // softmax warpgroup has stored the previous block's O_t
-            ok = wait(C::B_PFULL + tq, gi);
+            ok = wait(C::pfull(tq, b), gi / C::SBUF);
             if (!ok) break;
             tc_fence_after();
-            if (leader) issue_pv(tq, st, it > 0);
+            if (leader) issue_pv(tq, st, b, it > 0);
             if (leader) mma_commit(bar(C::B_OREADY + tq));
-            if (it + 1 < n) {
+            if (next) {
               if (tq == 0) {
-                ok = wait(C::B_KFULL + nst, (gi + 1) / C::STAGES);
+                ok = wait(C::B_KFULL + nst, gn / C::STAGES);
                 if (!ok) break;
                 tc_fence_after();
               }
-              if (leader) issue_s(tq, nst);
-              if (leader) mma_commit(bar(C::B_SFULL + tq));
+              if (leader) issue_s(tq, nst, b);  // after PV(gi) read P from buffer b
+              if (leader) mma_commit(bar(C::sfull(tq, b)));
             }
           }
           if (!ok) break;
-          if (it + 2 == n && leader) mma_commit(bar(C::B_QEMPTY));
-          if (it + 1 < n && leader) mma_commit(bar(C::B_KEMPTY + nst));  // K(it+1) read by its last S
-          if (leader) mma_commit(bar(C::B_VEMPTY + st));                 // V(it) read by its last PV
+          if (next && it + C::SBUF == n - 1 && leader) mma_commit(bar(C::B_QEMPTY));
+          if (next && leader) mma_commit(bar(C::B_KEMPTY + nst));  // K(gn) read by its last S
+          if (leader) mma_commit(bar(C::B_VEMPTY + st));          // V(gi) read by its last PV
         }
         if (!ok) break;
         gk += n;
@@ -298,7 +326,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const int quarter = warp & 3;               // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;          // row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_addr = tmem + lane_base + C::S_COL(tq);
     const uint32_t o_addr = tmem + lane_base + C::O_COL(tq);
     const float c = s.scale_log2;
     using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
@@ -313,7 +340,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       for (int it = 0; it < t.n_iter; ++it) {
         const int gi = gk + it;
         const int k0 = (t.j_lo + it) * C::BN;
-        ok = mbar_wait(bar(C::B_SFULL + tq), gi & 1, tmo, abort_flag, wc.status);
+        const int b = gi % C::SBUF;  // score buffer of this tile
+        const uint32_t s_addr = tmem + lane_base + C::S_COL(tq, b);
+        ok = mbar_wait(bar(C::sfull(tq, b)), (gi / C::SBUF) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         tc_fence_after();
         // one TMEM round trip for the whole row (a load issued while the tensor
@@ -369,7 +398,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const float rs = (a01.x + a01.y) + (a23.x + a23.y);
         l = l * alpha + rs;
         if (it > 0 && __any_sync(0xffffffffu, grow)) {
-          // O_t holds the sum of the previous tiles: wait for the last of them.
+          // O_t holds the sum of the previous tiles: wait for the last of them
+          // (PV(gi-2) has completed: S(gi), just read, was issued after it, so
+          // the barrier is at most one phase behind).
           ok = mbar_wait(bar(C::B_OREADY + tq), (gi - 1) & 1, tmo, abort_flag, wc.status);
           if (!ok) break;
           tc_fence_after();
@@ -386,7 +417,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_PFULL + tq));
+        if (lane == 0) mbar_arrive(bar(C::pfull(tq, b)));
       }
       if (!ok) break;
 
@@ -397,7 +428,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       // P, which comes after these reads.
       const bool have = t.n_iter > 0;
       if (have) {
-        ok = mbar_wait(bar(C::B_OREADY + tq), (gk + t.n_iter - 1) & 1, tmo, abort_flag, wc.status);
+        // O_t is final once the block's last PV completed. A parity wait is
+        // only sound when the barrier is at most one phase behind: with two
+        // score buffers the block's last S was issued before its second-to-last
+        // PV, which may still be running, so that PV is waited for first.
+        const int last = gk + t.n_iter - 1;
+        if (C::SBUF == 2 && t.n_iter > 1)
+          ok = mbar_wait(bar(C::B_OREADY + tq), (last - 1) & 1, tmo, abort_flag, wc.status);
+        ok = ok && mbar_wait(bar(C::B_OREADY + tq), last & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         tc_fence_after();
       }
