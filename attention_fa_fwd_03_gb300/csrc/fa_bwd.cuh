@@ -5,7 +5,7 @@
 //   pass 1  D_i = rowsum(dO_i o O_i) from the stored O           (fa_bwd_dvec_kernel)
 //   pass 2  per KV row block, over every query head of its group and every
 //           query tile: p = exp(s - L), dp = dO.v, ds = p (dp - D),
-//           dV += p dO, dK += ds q scale                          (fa_bwd_dkv_split_kernel)
+//           dV += p dO, dK += ds q scale                        (fa_bwd_dkv_split2_kernel)
 //   pass 3  per query row block, over key tiles: dQ += ds k scale (fa_bwd_dq_serial_kernel)
 // and page "[Metal] Add Flash Attention VJP for training", Implementation
 // Notes: two kernels instead of atomics, with the dK/dV kernel owning its KV
@@ -104,13 +104,17 @@ struct DkvSplitCfg {
   static_assert(BMQ == 64 || BMQ == 128, "query tile");
 };
 
+// One CTA of a pass over KV block `linear` of the grid order (the tensor maps
+// are the kernel's own parameters).
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1)
-fa_bwd_dkv_split_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-                  const float* __restrict__ lse, const float* __restrict__ dvec,
-                  void* __restrict__ dk_out, void* __restrict__ dv_out, float scale, AttnShape s,
-                  TileOrder order, WaitCfg wc) {
+__device__ __forceinline__ void dkv_split_body(const CUtensorMap& map_q, const CUtensorMap& map_k,
+                                               const CUtensorMap& map_v, const CUtensorMap& map_do,
+                                               const float* __restrict__ lse,
+                                               const float* __restrict__ dvec,
+                                               void* __restrict__ dk_out, void* __restrict__ dv_out,
+                                               float scale, const AttnShape& s,
+                                               const TileOrder& order, const WaitCfg& wc,
+                                               int linear) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -125,7 +129,7 @@ fa_bwd_dkv_split_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
   float* stats = reinterpret_cast<float*>(smem + C::OFF_STATS);  // [buf][lse2|dvec][BMQ]
 
   int bg, kvt;  // (b * Hkv + g, block of 128 KV rows)
-  decode_tile(blockIdx.x, order, &bg, &kvt);
+  decode_tile(linear, order, &bg, &kvt);
   const int b = bg / s.Hkv, g = bg % s.Hkv;
   const int reps = s.Hq / s.Hkv;
   const int k0 = kvt * kBM;
@@ -335,6 +339,25 @@ fa_bwd_dkv_split_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// Both passes in one grid: CTA 2u runs the dV pass and CTA 2u + 1 the dK pass
+// of KV block u, so the two passes of a block run side by side (twice the CTAs
+// in flight of two back-to-back launches, and their Q / dO reads share L2).
+template <class CV, class CK>
+__global__ void __launch_bounds__(CV::THREADS, 1)
+fa_bwd_dkv_split2_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                         const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                         const float* __restrict__ lse, const float* __restrict__ dvec,
+                         void* __restrict__ dk_out, void* __restrict__ dv_out, float scale,
+                         AttnShape s, TileOrder order, WaitCfg wc) {
+  static_assert(CV::THREADS == CK::THREADS && CV::BMQ == CK::BMQ, "one launch shape");
+  if ((blockIdx.x & 1) == 0)
+    dkv_split_body<CV>(map_q, map_k, map_v, map_do, lse, dvec, dk_out, dv_out, scale, s, order,
+                       wc, blockIdx.x >> 1);
+  else
+    dkv_split_body<CK>(map_q, map_k, map_v, map_do, lse, dvec, dk_out, dv_out, scale, s, order,
+                       wc, blockIdx.x >> 1);
 }
 
 // ------------------------------------------------------------------ pass 3: dQ

@@ -127,6 +127,26 @@ cudaError_t launch_dkv_with(const BwdLaunch& a, Kern kern) {
   return cudaGetLastError();
 }
 
+// The two D = 256 dK/dV passes as one grid (fa_bwd_dkv_split2_kernel).
+template <class CV, class CK>
+cudaError_t launch_dkv_split2(const BwdLaunch& a) {
+  const int bhq = a.s.B * a.s.Hq, bhkv = a.s.B * a.s.Hkv;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_tile_map(&mq, a.q, CV::BF16, CV::D, a.s.Tq, bhq, CV::BMQ) ||
+      !encode_tile_map(&mdo, a.dout, CV::BF16, CV::D, a.s.Tq, bhq, CV::BMQ) ||
+      !encode_tile_map(&mk, a.k, CV::BF16, CV::D, a.s.Tkv, bhkv, kBM) ||
+      !encode_tile_map(&mv, a.v, CV::BF16, CV::D, a.s.Tkv, bhkv, kBM))
+    return cudaErrorInvalidValue;
+  auto kern = fa_bwd_dkv_split2_kernel<CV, CK>;
+  const int smem = CV::SMEM_BYTES > CK::SMEM_BYTES ? CV::SMEM_BYTES : CK::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const TileOrder order = kv_block_order(a.s, CV::D);
+  kern<<<2 * order.units * order.tiles, CV::THREADS, smem, a.stream>>>(
+      mq, mk, mv, mdo, a.lse, a.dvec, a.dk, a.dv, a.scale, a.s, order, a.wc);
+  return cudaGetLastError();
+}
+
 template <class C, class Kern>
 cudaError_t launch_dq_with(const BwdLaunch& a, Kern kern) {
   const int bhq = a.s.B * a.s.Hq, bhkv = a.s.B * a.s.Hkv;
@@ -168,8 +188,7 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
     } else {
       using CV = DkvSplitCfg<D, 64, 2, BF16, kModeDV>;
       using CK = DkvSplitCfg<D, 64, 1, BF16, kModeDK>;
-      e = launch_dkv_with<CV>(a, fa_bwd_dkv_split_kernel<CV>);
-      if (e == cudaSuccess) e = launch_dkv_with<CK>(a, fa_bwd_dkv_split_kernel<CK>);
+      e = launch_dkv_split2<CV, CK>(a);
     }
   }
   if (e != cudaSuccess) return e;
