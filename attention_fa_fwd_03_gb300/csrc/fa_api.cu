@@ -283,6 +283,7 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   int hq = Hq, tq = Tq;
   fold_group_rows(causal, window, Hkv, 0, &hq, &tq);
   a.s = make_shape(B, hq, Hkv, tq, Tkv, causal, window, scale);
+  a.s_rows = make_shape(B, Hq, Hkv, Tq, Tkv, causal, window, scale);
   a.bf16 = dt == FA_BF16;
   if (!status_ptr(&a.wc.status)) return FA_ERR_LAUNCH;
   a.wc.timeout_cycles = wait_timeout_cycles();

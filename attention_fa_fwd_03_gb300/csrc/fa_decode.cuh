@@ -386,4 +386,258 @@ fa_fwd_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_con
   }
 }
 
+// ---------------------------------------------------------------------------
+// dQ for short query blocks (backward pass 3 of page "mlx-bun 0.0.4:
+// package/src/model/flash-attention.ts": dQ_i = scale * sum_j dS_ij K_j with
+// P_ij = exp(S_ij - L_i) from the cached LSE and dS_ij = P_ij (dP_ij - D_i),
+// dP_ij = dO_i . V_j), split over the keys like the forward above: one cluster
+// per (batch, query head), each CTA a slice of the keys staged by TMA, a lane
+// per key for S and dP, a lane per output column pair for dS K. No running max
+// is needed (LSE is known), so a CTA's partial dQ rows are plain sums; they
+// are pushed into the row owner's shared memory and added there after one
+// cluster barrier. Needs the D-vector of backward pass 1 (the workspace).
+template <int D_, int TQ_, bool BF16_>
+struct DecodeDqCfg {
+  static constexpr int D = D_;
+  static constexpr int TQ = TQ_;
+  static constexpr bool BF16 = BF16_;
+  static constexpr int NP = (D / 2 + 31) / 32;
+  static constexpr int SK = 32 * kDecodeWarps;
+  static constexpr int DP = (D + 63) / 64 * 64;
+  static constexpr int KREG = DP / 64;
+  static constexpr int REGION = SK * 128;
+  static constexpr int TILE = KREG * REGION;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_F = OFF_V + TILE;
+  static constexpr int F_Q = 0;                                // [TQ][D] q * scale * log2(e)
+  static constexpr int F_DO = F_Q + TQ * D;                    // [TQ][D] dO
+  static constexpr int F_NL = F_DO + TQ * D;                   // [TQ] -LSE * log2(e)
+  static constexpr int F_DV = F_NL + TQ;                       // [TQ] D-vector
+  static constexpr int F_P = F_DV + TQ;                        // [warps][TQ][32] dS of a key block
+  static constexpr int F_OW = F_P + kDecodeWarps * TQ * 32;    // [warps][TQ][D] warp partial dQ
+  static constexpr int RSLOTS = TQ + kDecodeMaxSplit;
+  static constexpr int F_R = F_OW + kDecodeWarps * TQ * D;     // [RSLOTS][D] pushed partial rows
+  static constexpr int F_END = F_R + RSLOTS * D;
+  static constexpr int SMEM_BYTES = OFF_F + F_END * 4 + 1024;
+  static_assert(TQ >= 1 && TQ <= kDecodeMaxTq, "query rows");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+template <class C>
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+fa_bwd_dq_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                        const uint16_t* __restrict__ q, const uint16_t* __restrict__ dout,
+                        const float* __restrict__ lse, const float* __restrict__ dvec,
+                        uint16_t* __restrict__ dq, float scale, AttnShape s, int split,
+                        int k_first, int k_last, int keys_per_cta, WaitCfg wc) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full;
+  __shared__ int abort_flag;
+  constexpr int D = C::D, TQ = C::TQ;
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  float* sm = reinterpret_cast<float*>(smem + C::OFF_F);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int bh = blockIdx.x / split;
+  const int b = bh / s.Hq;
+  const int g = (bh - b * s.Hq) / (s.Hq / s.Hkv);
+  const int zkv = b * s.Hkv + g;
+  const int Tq = s.Tq;
+  const int64_t q_row0 = static_cast<int64_t>(bh) * Tq;
+  const int kbeg = min(k_last, k_first + static_cast<int>(rank) * keys_per_cta);
+  const int kend = min(k_last, kbeg + keys_per_cta);
+  const int nstage = (kend - kbeg + C::SK - 1) / C::SK;
+  const uint64_t tmo = wc.timeout_cycles;
+  cluster_arrive_relaxed();  // waited for before the first store into a peer
+
+  auto issue = [&](int i) {
+    const uint32_t bar = smem_u32(&full);
+    mbar_arrive_expect_tx(bar, 2 * C::TILE);
+    for (int r = 0; r < C::KREG; ++r) {
+      tma_load_3d(sbase + C::OFF_K + r * C::REGION, &map_k, bar, r * 64, kbeg + i * C::SK, zkv);
+      tma_load_3d(sbase + C::OFF_V + r * C::REGION, &map_v, bar, r * 64, kbeg + i * C::SK, zkv);
+    }
+  };
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&full), 1);
+    fence_mbar_init();
+    if (nstage > 0) issue(0);
+  }
+  // query and dO rows (rows past Tq are zero), their LSE (exp2 domain) and D
+  for (int e = threadIdx.x; e < TQ * D; e += kDecodeThreads) {
+    const int i = e / D;
+    float xq = 0.f, xd = 0.f;
+    if (i < Tq) {
+      const int64_t at = (q_row0 + i) * D + (e - i * D);
+      xq = unpack2<C::BF16>(static_cast<uint32_t>(q[at])).x * s.scale_log2;
+      xd = unpack2<C::BF16>(static_cast<uint32_t>(dout[at])).x;
+    }
+    sm[C::F_Q + e] = xq;
+    sm[C::F_DO + e] = xd;
+  }
+  if (threadIdx.x < TQ) {
+    const int i = threadIdx.x;
+    float nl = -INFINITY, dv = 0.f;  // no visible key (or past Tq): P = 0
+    if (i < Tq) {
+      const float L = lse[q_row0 + i];
+      if (L != -INFINITY) nl = -L * kLog2e;
+      dv = dvec[q_row0 + i];
+    }
+    sm[C::F_NL + i] = nl;
+    sm[C::F_DV + i] = dv;
+  }
+  __syncthreads();
+
+  float acc[TQ][C::NP][2];
+#pragma unroll
+  for (int i = 0; i < TQ; ++i)
+#pragma unroll
+    for (int u = 0; u < C::NP; ++u) acc[i][u][0] = acc[i][u][1] = 0.f;
+  const float* qs = sm + C::F_Q;
+  const float* dos = sm + C::F_DO;
+  float* ps = sm + C::F_P + warp * TQ * 32;
+
+  int done = 0;
+#pragma unroll 1
+  for (int st = 0; st < nstage; ++st) {
+    const bool ok = mbar_wait(smem_u32(&full), st & 1, tmo, &abort_flag, wc.status);
+    if (!__syncthreads_and(ok)) break;
+    done = st + 1;
+    const uint32_t ks = sbase + C::OFF_K, vs = sbase + C::OFF_V;
+    const int blk = kbeg + st * C::SK + 32 * warp;
+    if (blk < kend) {
+      const int rr = 32 * warp + lane;
+      const bool in = blk + lane < kend;
+      // S and dP of key blk + lane against every query row (lane = key)
+      float sc[TQ], dp[TQ];
+#pragma unroll
+      for (int i = 0; i < TQ; ++i) sc[i] = dp[i] = 0.f;
+#pragma unroll 2
+      for (int c8 = 0; c8 < D / 8; ++c8) {
+        uint32_t wk[4], wv[4];
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(wk[0]), "=r"(wk[1]), "=r"(wk[2]), "=r"(wk[3])
+                     : "r"(ks + stage_offset(C::REGION, rr, c8 * 8)));
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(wv[0]), "=r"(wv[1]), "=r"(wv[2]), "=r"(wv[3])
+                     : "r"(vs + stage_offset(C::REGION, rr, c8 * 8)));
+        float kf[8], vf[8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 a = unpack2<C::BF16>(wk[t]), c = unpack2<C::BF16>(wv[t]);
+          kf[2 * t] = a.x;
+          kf[2 * t + 1] = a.y;
+          vf[2 * t] = c.x;
+          vf[2 * t + 1] = c.y;
+        }
+#pragma unroll
+        for (int i = 0; i < TQ; ++i) {
+          const float4 qa = *reinterpret_cast<const float4*>(qs + i * D + c8 * 8);
+          const float4 qb = *reinterpret_cast<const float4*>(qs + i * D + c8 * 8 + 4);
+          const float4 da = *reinterpret_cast<const float4*>(dos + i * D + c8 * 8);
+          const float4 db = *reinterpret_cast<const float4*>(dos + i * D + c8 * 8 + 4);
+          sc[i] = fmaf(qa.x, kf[0], sc[i]);
+          sc[i] = fmaf(qa.y, kf[1], sc[i]);
+          sc[i] = fmaf(qa.z, kf[2], sc[i]);
+          sc[i] = fmaf(qa.w, kf[3], sc[i]);
+          sc[i] = fmaf(qb.x, kf[4], sc[i]);
+          sc[i] = fmaf(qb.y, kf[5], sc[i]);
+          sc[i] = fmaf(qb.z, kf[6], sc[i]);
+          sc[i] = fmaf(qb.w, kf[7], sc[i]);
+          dp[i] = fmaf(da.x, vf[0], dp[i]);
+          dp[i] = fmaf(da.y, vf[1], dp[i]);
+          dp[i] = fmaf(da.z, vf[2], dp[i]);
+          dp[i] = fmaf(da.w, vf[3], dp[i]);
+          dp[i] = fmaf(db.x, vf[4], dp[i]);
+          dp[i] = fmaf(db.y, vf[5], dp[i]);
+          dp[i] = fmaf(db.z, vf[6], dp[i]);
+          dp[i] = fmaf(db.w, vf[7], dp[i]);
+        }
+      }
+      // dS = P (dP - D) with P = 2^(s c - LSE log2 e); hidden keys give 0
+#pragma unroll
+      for (int i = 0; i < TQ; ++i) {
+        int lo, hi;
+        visible_keys(s, i, blk, &lo, &hi);
+        const bool vis = in && i < Tq && lane >= lo && lane < hi;
+        const float nl = sm[C::F_NL + i];
+        const float p = (vis && nl != -INFINITY) ? exp2f(sc[i] + nl) : 0.f;
+        ps[i * 32 + lane] = p * (dp[i] - sm[C::F_DV + i]);
+      }
+      __syncwarp();
+      // dQ += dS K over the block's keys (lane = output column pairs)
+      const int nj = min(32, kend - blk);
+#pragma unroll 4
+      for (int jj = 0; jj < nj; ++jj) {
+        float dsj[TQ];
+#pragma unroll
+        for (int i = 0; i < TQ; ++i) dsj[i] = ps[i * 32 + jj];
+#pragma unroll
+        for (int u = 0; u < C::NP; ++u) {
+          const int pidx = lane + 32 * u;
+          if (pidx < D / 2) {
+            uint32_t w;
+            asm volatile("ld.shared.u32 %0, [%1];"
+                         : "=r"(w)
+                         : "r"(ks + stage_offset(C::REGION, 32 * warp + jj, 2 * pidx)));
+            const float2 kv = unpack2<C::BF16>(w);
+#pragma unroll
+            for (int i = 0; i < TQ; ++i) {
+              acc[i][u][0] = fmaf(dsj[i], kv.x, acc[i][u][0]);
+              acc[i][u][1] = fmaf(dsj[i], kv.y, acc[i][u][1]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+    }
+    __syncthreads();  // every warp is done with the stage
+    if (threadIdx.x == 0 && st + 1 < nstage) issue(st + 1);
+  }
+  // after a wait gave up: let a load still in flight land before the CTA exits
+  if (threadIdx.x == 0 && done < nstage) mbar_wait(smem_u32(&full), done & 1, tmo, nullptr, wc.status);
+
+  // warp partials, their sum per CTA pushed into the row owner's shared memory
+  float* ow = sm + C::F_OW + warp * TQ * D;
+#pragma unroll
+  for (int i = 0; i < TQ; ++i)
+#pragma unroll
+    for (int u = 0; u < C::NP; ++u) {
+      const int pidx = lane + 32 * u;
+      if (pidx < D / 2) {
+        ow[i * D + 2 * pidx] = acc[i][u][0];
+        ow[i * D + 2 * pidx + 1] = acc[i][u][1];
+      }
+    }
+  __syncthreads();
+  float* recv = sm + C::F_R;
+  cluster_wait();  // every CTA of the cluster is running
+  for (int e = threadIdx.x; e < Tq * D; e += kDecodeThreads) {
+    const int i = e / D;
+    float x = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) x += sm[C::F_OW + w * TQ * D + e];
+    const int slot = (i / split) * split + static_cast<int>(rank);
+    st_peer_f32(recv + slot * D + (e - i * D), static_cast<uint32_t>(i % split), x);
+  }
+  cluster_barrier();  // every partial row has landed in its owner's shared memory
+
+  using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
+  for (int i = static_cast<int>(rank); i < Tq; i += split) {
+    const float* rows = recv + (i / split) * split * D;
+    T16* out = reinterpret_cast<T16*>(dq) + (q_row0 + i) * D;
+    for (int d = threadIdx.x; d < D; d += kDecodeThreads) {
+      float x = 0.f;
+      for (int c = 0; c < split; ++c) x += rows[c * D + d];
+      if constexpr (C::BF16)
+        out[d] = __float2bfloat16_rn(x * scale);
+      else
+        out[d] = __float2half_rn(x * scale);
+    }
+  }
+}
+
 }  // namespace fa

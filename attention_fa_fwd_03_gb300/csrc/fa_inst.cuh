@@ -176,6 +176,10 @@ constexpr int kSoftmaxWarpgroups = 4;
 // (fa_bwd_pipelined.cuh). D = 256: the accumulators alone fill TMEM, so dV and
 // dK run as two passes with 64-row query tiles and dQ with 64-column key
 // tiles, one stage (fa_bwd.cuh).
+// dQ of short query blocks on the split-key kernel (defined below)
+template <int D, bool BF16>
+cudaError_t run_dq_decode(const BwdLaunch& a);
+
 template <int D, bool BF16>
 cudaError_t run_bwd(const BwdLaunch& a, int phases) {
   cudaError_t e = cudaSuccess;
@@ -193,6 +197,7 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
   }
   if (e != cudaSuccess) return e;
   if (phases & kPhaseDq) {
+    if (a.s_rows.Tq <= kDecodeMaxTq) return run_dq_decode<D, BF16>(a);
     if constexpr (D <= 128) {
       using C = DqCfg<D, BF16, kSoftmaxWarpgroups>;
       e = launch_dq_with<C>(a, fa_bwd_dq_kernel<C>);
@@ -204,40 +209,18 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
   return e;
 }
 
-// Short query blocks (Tq <= 8): the split-key kernel of fa_decode.cuh, one
+// Short query blocks (Tq <= 8): the split-key kernels of fa_decode.cuh, one
 // cluster of `split` CTAs per (batch, query head). The cluster size trades the
 // keys each CTA walks (nk / split) against the waves the clusters need: the
-// device runs at most M(split) such clusters at once (queried once per kernel
-// and size), so the estimated time is ceil(clusters / M(split)) * nk / split.
-// Slices are whole 32-key blocks; a cluster never has more CTAs than 32-key
-// blocks to give them.
-template <class C>
-cudaError_t launch_fwd_decode(const FwdLaunch& a) {
-  int k_first, k_last;
-  key_range(a.s, 0, a.s.Tq, &k_first, &k_last);
-  const int nk = k_last - k_first;
-  const int64_t units = static_cast<int64_t>(a.s.B) * a.s.Hq;
-  auto kern = fa_fwd_decode_kernel<C>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  CUtensorMap mk, mv;
-  const int bhkv = a.s.B * a.s.Hkv;
-  if (!encode_tile_map(&mk, a.k, C::BF16, C::D, a.s.Tkv, bhkv, C::SK) ||
-      !encode_tile_map(&mv, a.v, C::BF16, C::D, a.s.Tkv, bhkv, C::SK))
-    return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kDecodeThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // clusters of each size the device holds at once (per device, cached)
-  static int max_active[64][kDecodeMaxSplit + 1] = {};
+// device runs at most M(split) such clusters at once (queried once per kernel,
+// device and size, into `cache`), so the estimated time is
+// ceil(clusters / M(split)) * (nk / split + fixed work). Slices are whole
+// 32-key blocks; a cluster never has more CTAs than 32-key blocks to give them.
+// `cfg` holds the block size, shared memory and stream; `attr` its cluster
+// attribute, whose size is set here along with the grid.
+inline void decode_split(const void* kern, cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr,
+                         int (*cache)[kDecodeMaxSplit + 1], int64_t units, int nk, int* split_out,
+                         int* per_out) {
   int dev = 0;
   cudaGetDevice(&dev);
   const int blocks32 = std::max(1, (nk + 31) / 32);
@@ -245,15 +228,15 @@ cudaError_t launch_fwd_decode(const FwdLaunch& a) {
   double best = 0.0;
   for (int sz = 1; sz <= kDecodeMaxSplit; sz *= 2) {
     if (sz > 1 && sz > blocks32) break;
-    int m = dev >= 0 && dev < 64 ? max_active[dev][sz] : 0;
+    int m = dev >= 0 && dev < 64 ? cache[dev][sz] : 0;
     if (m == 0) {
-      cfg.gridDim = dim3(static_cast<unsigned>(sz), 1, 1);
-      attr[0].val.clusterDim.x = static_cast<unsigned>(sz);
-      if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess || m < 1) {
+      cfg->gridDim = dim3(static_cast<unsigned>(sz), 1, 1);
+      attr->val.clusterDim.x = static_cast<unsigned>(sz);
+      if (cudaOccupancyMaxActiveClusters(&m, kern, cfg) != cudaSuccess || m < 1) {
         cudaGetLastError();  // clear; this size is not used
         continue;
       }
-      if (dev >= 0 && dev < 64) max_active[dev][sz] = m;
+      if (dev >= 0 && dev < 64) cache[dev][sz] = m;
     }
     const double waves = static_cast<double>((units + m - 1) / m);
     const double cost = waves * ((nk + sz - 1) / sz + 64);  // + per-CTA fixed work, in keys
@@ -265,11 +248,88 @@ cudaError_t launch_fwd_decode(const FwdLaunch& a) {
   int per = (nk + split - 1) / split;
   per = std::max(32, (per + 31) / 32 * 32);
   split = std::max(1, (nk + per - 1) / per);
-  cfg.gridDim = dim3(static_cast<unsigned>(units * split), 1, 1);
-  attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+  cfg->gridDim = dim3(static_cast<unsigned>(units * split), 1, 1);
+  attr->val.clusterDim.x = static_cast<unsigned>(split);
+  *split_out = split;
+  *per_out = per;
+}
+
+// Launch configuration of a split-key kernel with cluster dimension x.
+inline void decode_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int smem,
+                          cudaStream_t stream) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->blockDim = dim3(kDecodeThreads, 1, 1);
+  cfg->dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg->stream = stream;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = 1;
+  attr->val.clusterDim.y = 1;
+  attr->val.clusterDim.z = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
+template <class C>
+cudaError_t launch_fwd_decode(const FwdLaunch& a) {
+  int k_first, k_last;
+  key_range(a.s, 0, a.s.Tq, &k_first, &k_last);
+  auto kern = fa_fwd_decode_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  CUtensorMap mk, mv;
+  const int bhkv = a.s.B * a.s.Hkv;
+  if (!encode_tile_map(&mk, a.k, C::BF16, C::D, a.s.Tkv, bhkv, C::SK) ||
+      !encode_tile_map(&mv, a.v, C::BF16, C::D, a.s.Tkv, bhkv, C::SK))
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  decode_config(&cfg, attr, C::SMEM_BYTES, a.stream);
+  static int max_active[64][kDecodeMaxSplit + 1] = {};
+  int split, per;
+  decode_split(reinterpret_cast<const void*>(kern), &cfg, attr, max_active,
+               static_cast<int64_t>(a.s.B) * a.s.Hq, k_last - k_first, &split, &per);
   return cudaLaunchKernelEx(&cfg, kern, mk, mv, static_cast<const uint16_t*>(a.q),
                             static_cast<uint16_t*>(a.o), a.lse, a.s, split, k_first, k_last, per,
                             a.wc);
+}
+
+// dQ of short query blocks, on the call's own (unfolded) shape; reads the
+// D-vector the first backward phase wrote.
+template <class C>
+cudaError_t launch_dq_decode(const BwdLaunch& a) {
+  const AttnShape& s = a.s_rows;
+  int k_first, k_last;
+  key_range(s, 0, s.Tq, &k_first, &k_last);
+  auto kern = fa_bwd_dq_decode_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  CUtensorMap mk, mv;
+  const int bhkv = s.B * s.Hkv;
+  if (!encode_tile_map(&mk, a.k, C::BF16, C::D, s.Tkv, bhkv, C::SK) ||
+      !encode_tile_map(&mv, a.v, C::BF16, C::D, s.Tkv, bhkv, C::SK))
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  decode_config(&cfg, attr, C::SMEM_BYTES, a.stream);
+  static int max_active[64][kDecodeMaxSplit + 1] = {};
+  int split, per;
+  decode_split(reinterpret_cast<const void*>(kern), &cfg, attr, max_active,
+               static_cast<int64_t>(s.B) * s.Hq, k_last - k_first, &split, &per);
+  return cudaLaunchKernelEx(&cfg, kern, mk, mv, static_cast<const uint16_t*>(a.q),
+                            static_cast<const uint16_t*>(a.dout), a.lse, a.dvec,
+                            static_cast<uint16_t*>(a.dq), a.scale, s, split, k_first, k_last, per,
+                            a.wc);
+}
+
+template <int D, bool BF16>
+cudaError_t run_dq_decode(const BwdLaunch& a) {
+  const int tq = a.s_rows.Tq;
+  if (tq <= 1) return launch_dq_decode<DecodeDqCfg<D, 1, BF16>>(a);
+  if (tq <= 2) return launch_dq_decode<DecodeDqCfg<D, 2, BF16>>(a);
+  if (tq <= 4) return launch_dq_decode<DecodeDqCfg<D, 4, BF16>>(a);
+  return launch_dq_decode<DecodeDqCfg<D, 8, BF16>>(a);
 }
 
 template <int D, bool BF16>

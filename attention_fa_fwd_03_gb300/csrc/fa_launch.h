@@ -26,7 +26,8 @@ struct BwdLaunch {
   void *dq, *dk, *dv;
   float* dvec;  // workspace: [B, Hq, Tq] fp32
   float scale;
-  AttnShape s;
+  AttnShape s;       // shape the tile kernels run (grouped heads may be folded into rows)
+  AttnShape s_rows;  // the call's own shape: Hq heads of Tq rows each
   bool bf16;
   WaitCfg wc;
   cudaStream_t stream;
