@@ -74,6 +74,8 @@ def load_peaks() -> dict:
 
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cuh"],
+    "fa_fwd_decode_kernel": ["fa_decode.cuh"],
+    "fa_bwd_dq_decode_kernel": ["fa_decode.cuh"],
     "fa_bwd_dvec_kernel": ["fa_bwd.cuh"],
     "fa_bwd_dkv_kernel": ["fa_bwd_pipelined.cuh", "fa_bwd.cuh"],
     "fa_bwd_dq_kernel": ["fa_bwd_pipelined.cuh", "fa_bwd.cuh"],
@@ -275,7 +277,7 @@ def run_ours(args, rank, world, local_rank):
     ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.Hq, w.Tq), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sc, ca, wi = w.scale, w.causal, w.window
-    n_dkv = 2 if w.D == 256 else 1          # D=256 runs dV and dK as two passes
+    n_dkv = 1  # one dK/dV launch per step (at D = 256 both passes share one grid)
 
     def step(ev):
         ev[0].record()
@@ -365,14 +367,24 @@ def run_ours(args, rank, world, local_rank):
     # ---- roofline of the dominant kernel
     peaks = load_peaks()
     pairs = w.B * w.Hq * visible_pairs_per_head(w)
-    names = ["fa_fwd_kernel", "fa_bwd_dvec_kernel", "fa_bwd_dkv_kernel", "fa_bwd_dq_kernel"]
+    # query blocks of at most 8 rows per head run the split-key CUDA-core
+    # forward and dQ kernels (latency- and HBM-bound: reported against HBM)
+    short = w.Tq <= 8
+    names = ["fa_fwd_decode_kernel" if short else "fa_fwd_kernel", "fa_bwd_dvec_kernel",
+             "fa_bwd_dkv_kernel", "fa_bwd_dq_decode_kernel" if short else "fa_bwd_dq_kernel"]
     avg_ms = [sum(p) / len(p) for p in phase_ms]
     # algorithmic work per launch: tensor FLOPs of each kernel's contractions over
-    # the visible pairs (2*D per pair per contraction), bytes for the D-vector pass
+    # the visible pairs (2*D per pair per contraction); bytes for the D-vector
+    # pass and the split-key kernels (K and V read once per query head, the
+    # head's query rows read and its output rows written)
+    row_bytes = w.B * w.Hq * w.Tq * w.D * 2
+    kv_bytes = w.B * w.Hq * w.Tkv * w.D * 2 * 2
     alg = {"fa_fwd_kernel": ("tensor", 2 * 2 * w.D * pairs),
+           "fa_fwd_decode_kernel": ("hbm", kv_bytes + 2 * row_bytes + w.B * w.Hq * w.Tq * 4),
            "fa_bwd_dvec_kernel": ("hbm", 2 * w.B * w.Hq * w.Tq * w.D * 2 + w.B * w.Hq * w.Tq * 4),
            "fa_bwd_dkv_kernel": ("tensor", 4 * 2 * w.D * pairs),
-           "fa_bwd_dq_kernel": ("tensor", 3 * 2 * w.D * pairs)}
+           "fa_bwd_dq_kernel": ("tensor", 3 * 2 * w.D * pairs),
+           "fa_bwd_dq_decode_kernel": ("hbm", kv_bytes + 3 * row_bytes + 2 * w.B * w.Hq * w.Tq * 4)}
     kernels = {}
     for nm, ms in zip(names, avg_ms):
         bound, work = alg[nm]
