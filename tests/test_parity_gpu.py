@@ -216,6 +216,8 @@ EDGE = [
     (3, 6, 3, 4, 5000, 128, "fp16", False, 0),       # long keys: 8-CTA clusters
     (1, 2, 1, 2, 33, 256, "fp16", False, 0),         # ragged key block, D=256
     (1, 16, 1, 3, 2000, 64, "bf16", False, 0),       # GQA 16:1
+    (1, 8, 1, 1, 20000, 128, "bf16", False, 0),      # decode over a long key range
+    (1, 4, 2, 8, 9000, 96, "fp16", False, 1000),     # long keys, window 1000 (past only)
     # mask-free GQA below one tile: the heads' rows share tiles
     (2, 8, 2, 40, 300, 128, "bf16", False, 0),       # 4 x 40 rows per group
     (1, 6, 2, 100, 200, 64, "fp16", False, 0),       # 3 x 100 rows, ragged tiles
