@@ -276,3 +276,33 @@ def test_full_size_runs_repeat_bit_for_bit():
         else:
             for n, t in outs.items():
                 assert torch.equal(t, first[n]), f"run {run}: {n} differs from the first run"
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tq,Tkv,D,dt,causal,window", [
+    (1, 4, 2, 300, 300, 128, "bf16", True, 0),       # tile kernels
+    (2, 8, 2, 4, 700, 128, "fp16", False, 0),        # short queries: folded dK/dV, split-key dQ
+    (1, 2, 1, 200, 200, 256, "bf16", True, 64),      # D = 256 kernels
+])
+def test_phase_calls_equal_fa_bwd(B, Hq, Hkv, Tq, Tkv, D, dt, causal, window):
+    """fa_bwd_preprocess + fa_bwd_dkv + fa_bwd_dq (the phases the benchmark
+    times one by one) give exactly what one fa_bwd call gives."""
+    m = fa()
+    w = fa_inputs.Workload("phases", B, Hq, Hkv, Tq, Tkv, D, dt, causal, window, seed=55)
+    x = fa_inputs.make_inputs(w)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    m.fa_fwd(q, k, v, o, lse, w.scale, causal, window)
+    ws = torch.empty(m.fa_bwd_workspace_size(B, Hq, Tq), dtype=torch.uint8, device=dev)
+    one = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+    m.fa_bwd(q, k, v, o, do, lse, *one, w.scale, causal, window, workspace=ws)
+    ws2 = torch.empty_like(ws)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    m.fa_bwd_preprocess(o, do, ws2)
+    m.fa_bwd_dkv(q, k, v, do, lse, ws2, dk, dv, w.scale, causal, window)
+    m.fa_bwd_dq(q, k, v, do, lse, ws2, dq, w.scale, causal, window)
+    torch.cuda.synchronize()
+    assert m.fa_device_status() == 0
+    for name, a, b in (("dq", one[0], dq), ("dk", one[1], dk), ("dv", one[2], dv)):
+        assert torch.equal(a, b), name
