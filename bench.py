@@ -72,6 +72,13 @@ def load_peaks() -> dict:
             "source": "fallback"}
 
 
+def workload_config(w) -> dict:
+    """The workload part of the JSON line's config, the same for both arms."""
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Tq": w.Tq, "Tkv": w.Tkv,
+            "D": w.D, "causal": w.causal, "window": w.window, "seed": w.seed,
+            "inputs": "seeded N(0,1), rounded to dtype"}
+
+
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cuh"],
     "fa_fwd_decode_kernel": ["fa_decode.cuh"],
@@ -464,12 +471,10 @@ def run_ours(args, rank, world, local_rank):
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Tq": w.Tq,
-                   "Tkv": w.Tkv, "D": w.D, "causal": w.causal, "window": w.window,
-                   "seed": w.seed, "inputs": "seeded N(0,1), rounded to dtype",
-                   "l2": "256 MiB buffer written between timed steps (outside the step's events); "
-                         "step working set > L2",
-                   "parallelism": f"replicas x{world} (each GPU runs the full workload, no collective)"},
+        "config": dict(workload_config(w),
+                       l2="256 MiB buffer written between timed steps (outside the step's events); "
+                          "step working set > L2",
+                       parallelism=f"replicas x{world} (each GPU runs the full workload, no collective)"),
         "pct_of_nominal_bf16_peak": round(100 * value / world / NOMINAL_BF16_TFLOPS, 2),
         "pct_of_measured_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
         "fwd_tflops": round(fwd_f / (fwd_ms / 1e3) / 1e12, 2),
@@ -511,8 +516,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_s * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Tq": w.Tq,
-                   "Tkv": w.Tkv, "D": w.D, "causal": w.causal, "window": w.window},
+        "config": workload_config(w),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
