@@ -6,6 +6,7 @@
 // "R/ag_flash_attn.R" (ggmlR), the f32-only backward note: an abort inside the
 // library took the whole session down, so every shape error is reported to
 // the caller instead).
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -128,13 +129,16 @@ bool encode_tile_map(CUtensorMap* map, const void* base, bool bf16, int D, int T
 }
 
 int device_sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64] = {};  // callers on several host threads share it
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 1;
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "fa_bwd.cuh"
@@ -219,7 +220,8 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
 // `cfg` holds the block size, shared memory and stream; `attr` its cluster
 // attribute, whose size is set here along with the grid.
 inline void decode_split(const void* kern, cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr,
-                         int (*cache)[kDecodeMaxSplit + 1], int64_t units, int nk, int* split_out,
+                         std::atomic<int> (*cache)[kDecodeMaxSplit + 1], int64_t units, int nk,
+                         int* split_out,
                          int* per_out) {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -228,7 +230,7 @@ inline void decode_split(const void* kern, cudaLaunchConfig_t* cfg, cudaLaunchAt
   double best = 0.0;
   for (int sz = 1; sz <= kDecodeMaxSplit; sz *= 2) {
     if (sz > 1 && sz > blocks32) break;
-    int m = dev >= 0 && dev < 64 ? cache[dev][sz] : 0;
+    int m = dev >= 0 && dev < 64 ? cache[dev][sz].load(std::memory_order_relaxed) : 0;
     if (m == 0) {
       cfg->gridDim = dim3(static_cast<unsigned>(sz), 1, 1);
       attr->val.clusterDim.x = static_cast<unsigned>(sz);
@@ -236,7 +238,7 @@ inline void decode_split(const void* kern, cudaLaunchConfig_t* cfg, cudaLaunchAt
         cudaGetLastError();  // clear; this size is not used
         continue;
       }
-      if (dev >= 0 && dev < 64) cache[dev][sz] = m;
+      if (dev >= 0 && dev < 64) cache[dev][sz].store(m, std::memory_order_relaxed);
     }
     const double waves = static_cast<double>((units + m - 1) / m);
     const double cost = waves * ((nk + sz - 1) / sz + 64);  // + per-CTA fixed work, in keys
@@ -285,7 +287,7 @@ cudaError_t launch_fwd_decode(const FwdLaunch& a) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   decode_config(&cfg, attr, C::SMEM_BYTES, a.stream);
-  static int max_active[64][kDecodeMaxSplit + 1] = {};
+  static std::atomic<int> max_active[64][kDecodeMaxSplit + 1] = {};  // shared by host threads
   int split, per;
   decode_split(reinterpret_cast<const void*>(kern), &cfg, attr, max_active,
                static_cast<int64_t>(a.s.B) * a.s.Hq, k_last - k_first, &split, &per);
@@ -313,7 +315,7 @@ cudaError_t launch_dq_decode(const BwdLaunch& a) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   decode_config(&cfg, attr, C::SMEM_BYTES, a.stream);
-  static int max_active[64][kDecodeMaxSplit + 1] = {};
+  static std::atomic<int> max_active[64][kDecodeMaxSplit + 1] = {};  // shared by host threads
   int split, per;
   decode_split(reinterpret_cast<const void*>(kern), &cfg, attr, max_active,
                static_cast<int64_t>(s.B) * s.Hq, k_last - k_first, &split, &per);
