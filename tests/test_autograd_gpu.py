@@ -40,6 +40,8 @@ CASES = [
     ("c1_b1_h2x1_t64_d64_fp16_causal", None),
     (None, fa_inputs.Workload("ag_gqa_window", 1, 4, 2, 300, 300, 128, "bf16", True, 64, seed=41)),
     (None, fa_inputs.Workload("ag_cross", 2, 4, 1, 90, 200, 96, "fp16", False, 0, seed=42)),
+    # decode-shaped: split-key forward and dQ, folded dK/dV
+    (None, fa_inputs.Workload("ag_short", 2, 8, 2, 4, 600, 128, "bf16", False, 0, seed=45)),
 ]
 
 
