@@ -165,3 +165,50 @@ def test_binding_without_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(fa, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         fa.library()
+
+
+def call_dkv(lib, p=None, **kw):
+    a = dict(GOOD, **kw)
+    p = p or ptrs(8)
+    return lib.fa_bwd_dkv(*p, a["B"], a["Hq"], a["Hkv"], a["Tq"], a["Tkv"], a["D"], a["scale"],
+                          a["causal"], a["window"], a["dt"], None)
+
+
+def call_dq(lib, p=None, **kw):
+    a = dict(GOOD, **kw)
+    p = p or ptrs(7)
+    return lib.fa_bwd_dq(*p, a["B"], a["Hq"], a["Hkv"], a["Tq"], a["Tkv"], a["D"], a["scale"],
+                         a["causal"], a["window"], a["dt"], None)
+
+
+@pytest.mark.parametrize("kw,code", BAD_ARGS)
+def test_backward_phases_reject_bad_arguments(lib, kw, code):
+    """The phase entry points validate like fa_bwd, before any launch."""
+    assert call_dkv(lib, **kw) == code
+    assert call_dq(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [(dict(B=0), INVALID), (dict(Tq=0), INVALID),
+                                     (dict(D=80), HEAD_DIM), (dict(dt=5), DTYPE)])
+def test_preprocess_rejects_bad_arguments(lib, kw, code):
+    a = dict(GOOD, **kw)
+    p = ptrs(3)
+    assert lib.fa_bwd_preprocess(*p, a["B"], a["Hq"], a["Tq"], a["D"], a["dt"], None) == code
+
+
+def test_noalloc_rejects_too_many_rows(lib):
+    """fa_bwd_noalloc keeps the D-vector in a fixed array: more rows than it
+    holds is an argument error, reported before anything is launched."""
+    f = lib.fa_bwd_noalloc
+    vp, i, fl = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    f.argtypes = [vp] * 9 + [i] * 6 + [fl, i, i, i, vp]
+    f.restype = i
+    lib.fa_bwd_noalloc_max_rows.restype = ctypes.c_size_t
+    rows = int(lib.fa_bwd_noalloc_max_rows())
+    a = dict(GOOD, B=1, Hq=2, Hkv=1, Tq=rows // 2 + 1)
+    assert f(*ptrs(9), a["B"], a["Hq"], a["Hkv"], a["Tq"], a["Tkv"], a["D"], a["scale"],
+             a["causal"], a["window"], a["dt"], None) == INVALID
+    for kw, code in BAD_ARGS[:10]:
+        a = dict(GOOD, **kw)
+        assert f(*ptrs(9), a["B"], a["Hq"], a["Hkv"], a["Tq"], a["Tkv"], a["D"], a["scale"],
+                 a["causal"], a["window"], a["dt"], None) == code, kw
