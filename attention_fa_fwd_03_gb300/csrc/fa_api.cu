@@ -146,10 +146,6 @@ int device_sm_count() {
 
 using namespace fa;
 
-extern "C" {
-
-}  // extern "C"
-
 namespace fa_selftest {
 
 // Two warps, two mbarriers that never complete (count 2, one arrival). Warp 0
@@ -374,10 +370,42 @@ namespace {
 // Largest B * Hq * Tq the array holds: 2^20 fp32 values (4 MiB).
 constexpr size_t kNoallocMaxRows = size_t(1) << 20;
 
-// Device addresses of the array, found once per device (with that device
-// current) on the first fa_bwd_noalloc call made there.
+// Device address of the array, looked up once per device with that device
+// current, and kept together with the id of the CUDA context it belongs to.
+// A device reset (cudaDeviceReset) destroys that context and with it the
+// address; the next call then runs in a new context with another id and looks
+// the address up again instead of launching against freed memory.
+struct NoallocSlot {
+  unsigned long long ctx_id;
+  float* ptr;
+};
 std::mutex g_noalloc_mutex;
-float* g_noalloc_ptr[64] = {nullptr};
+NoallocSlot g_noalloc_slot[64] = {};
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+void load_ctx_calls() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+          cudaSuccess && q == cudaDriverEntryPointSuccess)
+    g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess && q == cudaDriverEntryPointSuccess)
+    g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+}
+
+// Id of the context current on this thread (0 when none is current yet).
+bool current_ctx_id(unsigned long long* id) {
+  *id = 0;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return false;
+  if (ctx == nullptr) return true;
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -386,15 +414,24 @@ static __device__ __align__(256) float g_noalloc_scratch[kNoallocMaxRows];
 namespace {
 
 fa_status noalloc_scratch(float** out) {
+  std::call_once(g_ctx_once, load_ctx_calls);
+  if (!g_ctx_current || !g_ctx_id) return FA_ERR_LAUNCH;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA_ERR_LAUNCH;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
+  unsigned long long id = 0;
+  if (!current_ctx_id(&id)) return FA_ERR_LAUNCH;
+  NoallocSlot& slot = g_noalloc_slot[dev];
+  if (slot.ptr == nullptr || id == 0 || slot.ctx_id != id) {
+    // set-up on this device (and context): the runtime creates the context
+    // if none is current yet
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FA_ERR_LAUNCH;
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
+    if (!current_ctx_id(&id) || id == 0) return FA_ERR_LAUNCH;
+    slot.ptr = static_cast<float*>(p);
+    slot.ctx_id = id;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = slot.ptr;
   return FA_OK;
 }
 

@@ -72,11 +72,33 @@ def load_peaks() -> dict:
             "source": "fallback"}
 
 
+L2_NOTE = ("GPU arm: a 256 MiB buffer is written between timed steps (outside the step's "
+           "events), and the step's working set exceeds the 126 MiB L2")
+
+# A timed region at least this long runs the GPU under its power cap: the
+# roofline then uses the sustained bf16 peak, otherwise the burst peak.
+SUSTAINED_REGION_S = 2.0
+
+
 def workload_config(w) -> dict:
-    """The workload part of the JSON line's config, the same for both arms."""
+    """The JSON line's config: the workload and the L2 rule, the same for both
+    arms (how many GPUs run it is the line's n_gpus / parallelism)."""
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Tq": w.Tq, "Tkv": w.Tkv,
             "D": w.D, "causal": w.causal, "window": w.window, "seed": w.seed,
-            "inputs": "seeded N(0,1), rounded to dtype"}
+            "inputs": "seeded N(0,1), rounded to dtype", "l2": L2_NOTE}
+
+
+def roofline_peak(peaks: dict, region_s: float) -> tuple[float, str]:
+    """The bf16 peak a tensor-bound kernel is measured against: the sustained
+    figure when the timed region lasts SUSTAINED_REGION_S or more (the clocks
+    settle under the power cap), the burst figure for a shorter region."""
+    if region_s >= SUSTAINED_REGION_S and peaks.get("bf16_tflops_sustained"):
+        return peaks["bf16_tflops_sustained"], (
+            f"{peaks['source']} sustained bf16 (timed region {region_s:.2f} s >= "
+            f"{SUSTAINED_REGION_S:.0f} s)")
+    return peaks["bf16_tflops"], (
+        f"{peaks['source']} burst bf16 (timed region {region_s:.2f} s < "
+        f"{SUSTAINED_REGION_S:.0f} s)")
 
 
 KERNEL_SOURCES = {
@@ -438,20 +460,22 @@ def run_ours(args, rank, world, local_rank):
     launches = n_dkv if dom == "fa_bwd_dkv_kernel" else 1
     launch_s = avg_ms[names.index(dom)] / launches / 1e3
     work_per_launch = work / launches
+    region_s = sum(step_ms) / 1e3
     if bound == "tensor":
         achieved = work_per_launch / launch_s / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        peak, peak_source = roofline_peak(peaks, region_s)
         unit = "TFLOP/s"
     else:
         achieved = work_per_launch / launch_s / 1e9
-        peak = peaks["hbm_gbs"]
+        peak, peak_source = peaks["hbm_gbs"], f"{peaks['source']} HBM copy"
         unit = "GB/s"
     traffic = ncu_traffic(dom, w.name)
     roofline = {"kernel": dom, "bound": bound, "achieved": round(achieved, 2), "peak": peak,
                 "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
-                "peak_source": f"{peaks['source']} (sustained bf16: kernel timed inside a "
-                               "continuous multi-step loop)" if bound == "tensor" else peaks["source"],
+                "peak_source": peak_source,
                 "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4) if bound == "tensor" else None,
+                "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
+                                      if bound == "tensor" else None),
                 "work_per_launch": work_per_launch,
                 "work_definition": "tensor FLOPs of the kernel's own contractions over the visible "
                                    "(query, key) pairs: 2*D per pair per contraction (fwd 2, dK/dV 4, dQ 3)"}
@@ -471,10 +495,8 @@ def run_ours(args, rank, world, local_rank):
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": dict(workload_config(w),
-                       l2="256 MiB buffer written between timed steps (outside the step's events); "
-                          "step working set > L2",
-                       parallelism=f"replicas x{world} (each GPU runs the full workload, no collective)"),
+        "config": workload_config(w),
+        "parallelism": f"replicas x{world} (each GPU runs the full workload, no collective)",
         "pct_of_nominal_bf16_peak": round(100 * value / world / NOMINAL_BF16_TFLOPS, 2),
         "pct_of_measured_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
         "fwd_tflops": round(fwd_f / (fwd_ms / 1e3) / 1e12, 2),
@@ -514,6 +536,10 @@ def run_reference(args):
         "metric": "attention fwd+bwd TFLOP/s at 1 GB300 (and % of dense bf16 peak)",
         "impl": "reference", "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_s * 1e3, 1),
+        "ms_per_step_extrapolated": True,
+        "ms_per_step_method": ("each step times the oracle on a bounded sample (a query-row range "
+                               "of one (batch, KV group) slice) and scales it to the full workload "
+                               "by visible (query, key) pairs; not a measured full step"),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": workload_config(w),

@@ -143,10 +143,13 @@ fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
  * The array is one per device, shared by every call on that device and kept
  * until the process exits; it holds the last call's D-vector. Calls whose
  * launches overlap on the GPU (two streams, or two host threads) race on it:
- * keep them ordered on one stream. The first call on a device looks up the
- * array's device address (with that device current); make that first call
- * before any stream capture. Nothing in the array has to start at zero: each
- * call rewrites the part it uses before reading it. */
+ * keep them ordered on one stream. The first call on a device (with that
+ * device current) looks up the array's device address, which is set-up work:
+ * make that first call before any stream capture. The address belongs to the
+ * device's CUDA context; after cudaDeviceReset() the next call finds a new
+ * context and looks the address up again (so, after a reset, that call is
+ * again a first call). Nothing in the array has to start at zero: each call
+ * rewrites the part it uses before reading it. */
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                          const void* dO, const float* lse, void* dq, void* dk, void* dv,
                          int B, int Hq, int Hkv, int Tq, int Tkv, int D, float scale,

@@ -7,12 +7,13 @@ Tolerances (the headline requirement for fp16/bf16 inputs): O max-abs error
 
 Small workloads are compared in full (or on whole (batch, KV group) slices,
 which are independent problems). The two large workloads run at full size in
-the same launch configuration the benchmark times; their outputs are compared
-on sampled query-row ranges of one group, where the oracle is exact: O, LSE
-and dQ on every sampled row, and dK/dV on key rows whose visible query rows
-all lie in the sampled range. Properties that hold at any size (no NaN, each
-dK column block sums to zero over keys, dV sums to the group's dO) cover the
-rest of the output.
+the same launch configuration the benchmark times, and whole (batch, KV
+group) slices of their outputs are compared with the oracle on every row:
+four of the 32 groups of the causal B4 Hq32 Hkv8 T4096 workload (first,
+middle and last of the grid), and both groups (the whole output) of the
+sliding-window B1 Hq16 Hkv2 T16384 workload. Their gradients are checked per
+128-row block as well. Properties that hold at any size (no NaN, each dK
+column sums to zero over keys, dV sums to the group's dO) cover every group.
 """
 import math
 
@@ -142,52 +143,87 @@ def test_c5e_short_queries_full(name):
     compare_full(fa_inputs.WORKLOADS[name])
 
 
-def check_large_sampled(w, head_rows=256, tail_rows=256, groups=((0, 0),)):
+def run_gpu_device(x, w):
+    """fwd + bwd on the GPU at full size; outputs stay on the device."""
+    m = fa()
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    out = {"o": torch.empty_like(q), "lse": torch.empty(q.shape[:3], dtype=torch.float32, device=dev),
+           "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v)}
+    for t in out.values():
+        t.fill_(float("nan"))
+    ws = torch.empty(m.fa_bwd_workspace_size(*q.shape[:3]), dtype=torch.uint8, device=dev)
+    m.fa_fwd(q, k, v, out["o"], out["lse"], w.scale, w.causal, w.window)
+    m.fa_bwd(q, k, v, out["o"], do, out["lse"], out["dq"], out["dk"], out["dv"], w.scale,
+             w.causal, w.window, workspace=ws)
+    torch.cuda.synchronize()
+    assert m.fa_device_status() == 0, "a bounded device wait gave up"
+    return out
+
+
+def check_row_blocks(got, ref, what, rows=128):
+    """Relative Frobenius error of every block of `rows` rows (the last axis
+    but one): a wrong block cannot hide behind the norm of a whole slice."""
+    T = ref.shape[-2]
+    worst = 0.0
+    for r0 in range(0, T, rows):
+        e = rel_fro(got[..., r0:r0 + rows, :], ref[..., r0:r0 + rows, :])
+        assert e <= GRAD_TOL, f"{what}: rows [{r0}, {min(T, r0 + rows)}) rel-Frobenius {e:.3e}"
+        worst = max(worst, e)
+    return worst
+
+
+def check_large_groups(w, groups):
+    """Full-size run in the benchmark's launch configuration; whole (batch,
+    KV group) slices compared with the oracle on every row of every output:
+    O, LSE and dQ of the group's query heads, dK and dV of its KV head. The
+    gradients are also checked block by block (128 rows), and properties that
+    hold at any size cover the groups not compared."""
     x = fa_inputs.make_inputs(w)
-    got = run_gpu(x, w)
+    got = run_gpu_device(x, w)
+    for name, t in got.items():
+        nf = ~torch.isfinite(t)
+        if name == "lse":
+            nf &= ~torch.isneginf(t)
+        assert not bool(nf.any()), f"{w.name}: {int(nf.sum())} non-finite values in {name}"
     reps = w.Hq // w.Hkv
-    bad = {}
-    for name in ("o", "lse", "dq", "dk", "dv"):
-        nf = ~np.isfinite(got[name])
-        if nf.any():
-            where = np.argwhere(nf.reshape(nf.shape[0], nf.shape[1], nf.shape[2], -1).any(axis=3))
-            bad[name] = (int(nf.sum()), where[:8].tolist())
-    assert not bad, f"non-finite values (count, first [b, h, row]): {bad}"
     for (b, g) in groups:
-        xs = as64(group_views(x, b, g, reps))
+        xs = group_views(x, b, g, reps)
+        ref = oracle.attn_bwd(*as64(xs), w.scale, w.causal, w.window)
         h0, h1 = g * reps, (g + 1) * reps
-        # head rows: O, LSE, dQ exact
-        ref = oracle.attn_bwd(*xs, w.scale, w.causal, w.window, row_lo=0, row_hi=head_rows)
-        check_fwd(got["o"][b, h0:h1, :head_rows], got["lse"][b, h0:h1, :head_rows],
-                  ref["o"][0, :, :head_rows], ref["lse"][0, :, :head_rows], f"{w.name} head rows")
-        e = rel_fro(got["dq"][b, h0:h1, :head_rows], ref["dq"][0, :, :head_rows])
-        assert e <= GRAD_TOL, f"dq head rows {e:.3e}"
-        # tail rows: O, LSE, dQ exact; dK/dV exact for keys >= Tq - tail_rows (causal)
-        lo = w.Tq - tail_rows
-        ref = oracle.attn_bwd(*xs, w.scale, w.causal, w.window, row_lo=lo, row_hi=w.Tq)
-        check_fwd(got["o"][b, h0:h1, lo:], got["lse"][b, h0:h1, lo:],
-                  ref["o"][0, :, lo:], ref["lse"][0, :, lo:], f"{w.name} tail rows")
-        for n, gv, rv in (("dq", got["dq"][b, h0:h1, lo:], ref["dq"][0, :, lo:]),
-                          ("dk", got["dk"][b, g, lo:], ref["dk"][0, 0, lo:]),
-                          ("dv", got["dv"][b, g, lo:], ref["dv"][0, 0, lo:])):
-            e = rel_fro(gv, rv)
-            assert e <= GRAD_TOL, f"{w.name} {n} tail rows rel-Frobenius {e:.3e}"
-    # any-size properties: softmax rows sum to one / dS rows sum to zero
-    dk_sum = got["dk"].sum(axis=2)
-    assert np.abs(dk_sum).max() <= 1e-2 * np.abs(got["dk"]).sum(axis=2).max() + 1e-3
-    want_dv = x["do"].double().numpy().reshape(w.B, w.Hkv, reps, w.Tq, w.D).sum(axis=(2, 3))
-    got_dv = got["dv"].sum(axis=2)
-    assert rel_fro(got_dv, want_dv) <= 1e-2
+        sl = {"o": got["o"][b:b + 1, h0:h1], "lse": got["lse"][b:b + 1, h0:h1],
+              "dq": got["dq"][b:b + 1, h0:h1], "dk": got["dk"][b:b + 1, g:g + 1],
+              "dv": got["dv"][b:b + 1, g:g + 1]}
+        sl = {n: t.double().cpu().numpy() for n, t in sl.items()}
+        what = f"{w.name} b{b} g{g}"
+        o_err, lse_err = check_fwd(sl["o"], sl["lse"], ref["o"], ref["lse"], what)
+        errs = check_grads(sl, ref, what)
+        blk = {n: check_row_blocks(sl[n], ref[n], f"{what} {n}") for n in ("dq", "dk", "dv")}
+        print(f"{what}: O max-abs {o_err:.2e}, LSE {lse_err:.2e}, rel-Frobenius "
+              + ", ".join(f"{n} {errs[n]:.2e} (worst block {blk[n]:.2e})" for n in errs))
+    # any-size properties over every group: the rows of dS sum to zero, so each
+    # dK column sums to zero over the keys; the rows of P sum to one, so dV
+    # summed over the keys is the group's dO summed over its rows
+    dk = got["dk"].double()
+    dk_sum = dk.sum(dim=2)
+    assert float(dk_sum.abs().max()) <= 1e-2 * float(dk.abs().sum(dim=2).max()) + 1e-3
+    want_dv = x["do"].double().reshape(w.B, w.Hkv, reps, w.Tq, w.D).sum(dim=(2, 3))
+    got_dv = got["dv"].double().sum(dim=2).cpu()
+    assert rel_fro(got_dv.numpy(), want_dv.numpy()) <= 1e-2
 
 
-def test_c3_headline_full_size_sampled():
-    check_large_sampled(fa_inputs.WORKLOADS["c3_b4_h32x8_t4096_d128_bf16_causal"],
-                        groups=((0, 0), (3, 7)))
+def test_c3_headline_full_size_whole_groups():
+    """B4 Hq32 Hkv8 T4096 D128 bf16 causal: four whole (batch, KV group)
+    slices, at the start, in the middle and at the end of the grid."""
+    check_large_groups(fa_inputs.WORKLOADS["c3_b4_h32x8_t4096_d128_bf16_causal"],
+                       groups=((0, 0), (1, 3), (2, 5), (3, 7)))
 
 
-def test_c4_sliding_window_full_size_sampled():
-    check_large_sampled(fa_inputs.WORKLOADS["c4_b1_h16x2_t16384_d128_bf16_causal_w4096"],
-                        groups=((0, 1),))
+def test_c4_sliding_window_full_size_every_group():
+    """B1 Hq16 Hkv2 T16384 D128 bf16 causal, window 4096: both KV groups,
+    i.e. the whole output, compared with the oracle."""
+    check_large_groups(fa_inputs.WORKLOADS["c4_b1_h16x2_t16384_d128_bf16_causal_w4096"],
+                       groups=((0, 0), (0, 1)))
 
 
 # --------------------------------------------------------------- edge cases
