@@ -560,36 +560,60 @@ __device__ __forceinline__ DqItem dq_item(int linear, const TileOrder& o, const 
   return t;
 }
 
-template <int D_, bool BF16_, int NWG_>
+// Tile configuration of the dQ kernel. BN key rows per tile (N of S and dP),
+// NWG softmax warpgroups of 32 key columns each, K / V rings of KST / VST
+// tiles, and where Q sits:
+//  * D <= 128: Q and dO in shared memory, 128-key tiles, four warpgroups,
+//    rings 3 / 2, two dP blocks in TMEM.
+//  * D = 256 (QTM): the dQ accumulator takes 256 TMEM columns and a 128-row
+//    Q or dO tile 64 KB of shared memory. Q is kept in TMEM instead, as the A
+//    operand of S = Q K^T (the softmax warps write each item's Q rows there),
+//    which leaves shared memory for dO and 64-key K / V rings of 3 / 2 tiles.
+//    TMEM then holds two 64-column score blocks, Q and dQ (128 + 128 + 256
+//    columns): tile j computes S into block j % 2, and dP into the same block
+//    once the softmax has read S from it.
+template <int D_, bool BF16_, int NWG_, int BN_ = 128, int KST_ = 3, int VST_ = 2,
+          bool QTM_ = false>
 struct DqCfg {
   static constexpr int D = D_;
   static constexpr bool BF16 = BF16_;
   static constexpr int NWG = NWG_;
-  static constexpr int CW = 128 / NWG;  // key columns per softmax warpgroup
-  static constexpr int KST = 3;         // K ring: needed first by the next tile
-  static constexpr int VST = 2;         // V ring
-  static constexpr int BN = 128;        // key rows per tile (N of S, dP)
+  static constexpr int BN = BN_;        // key rows per tile (N of S, dP)
+  static constexpr int CW = BN / NWG;   // key columns per softmax warpgroup
+  static constexpr int KST = KST_;      // K ring: needed first by the next tile
+  static constexpr int VST = VST_;      // V ring
+  static constexpr bool QTM = QTM_;     // Q in TMEM (A operand of S from TMEM)
   static constexpr int DP = (D + 63) / 64 * 64;
   static constexpr int KREG = DP / 64;
-  static constexpr int REGION = 128 * 128;
-  static constexpr int TILE = KREG * REGION;
+  static constexpr int Q_REGION = 128 * 128;   // one 64-column block of a 128-row Q / dO tile
+  static constexpr int KV_REGION = BN * 128;   // one 64-column block of a K / V tile
+  static constexpr int Q_TILE = KREG * Q_REGION;
+  static constexpr int KV_TILE = KREG * KV_REGION;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = OFF_Q + TILE;
-  static constexpr int OFF_K = OFF_DO + TILE;
-  static constexpr int OFF_V = OFF_K + KST * TILE;
-  static constexpr int OFF_BAR = OFF_V + VST * TILE;
+  static constexpr int OFF_DO = OFF_Q + (QTM ? 0 : Q_TILE);
+  static constexpr int OFF_K = OFF_DO + Q_TILE;
+  static constexpr int OFF_V = OFF_K + KST * KV_TILE;
+  static constexpr int OFF_BAR = OFF_V + VST * KV_TILE;
   // barriers: q_full, q_empty, do_full, do_empty, k_full[KST], k_empty[KST],
-  // v_full[VST], v_empty[VST], s_full, s_free, dp_full[2], p_full[2], done,
-  // drain. p_full alternates with the tile's parity: S and dP of tile j+1 are
-  // issued before the MMA waits for dS(j), so one softmax warp can finish
-  // tile j+1 while another still works on tile j; with a single barrier its
-  // second arrival would complete tile j's phase early. Two tiles ahead is
-  // impossible (S(j+2) waits for every warp's s_free of tile j+1).
+  // v_full[VST], v_empty[VST], s_full[2], s_free, dp_full[2], p_full[2], done,
+  // drain.
+  // * p_full alternates with the tile's parity: with Q in shared memory, S and
+  //   dP of tile j+1 are issued before the MMA waits for dS(j), so one softmax
+  //   warp can finish tile j+1 while another still works on tile j; with a
+  //   single barrier its second arrival would complete tile j's phase early.
+  //   Two tiles ahead is impossible (S(j+2) waits for every warp's s_free of
+  //   tile j+1).
+  // * s_full[1] is used with Q in TMEM only, where S alternates between two
+  //   blocks: S(j+1) may complete before a slow softmax warp has waited for
+  //   S(j), so each block has its own barrier (S(j+2) waits for that warp's
+  //   dS(j)). s_free then gates dP(j), which goes into S(j)'s block.
+  // * With Q in TMEM, q_full counts one arrival per softmax warp (the warps
+  //   that write Q there) and q_empty is unused.
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_DOFULL = 2, B_DOEMPTY = 3, B_KFULL = 4,
                        B_KEMPTY = B_KFULL + KST, B_VFULL = B_KEMPTY + KST,
                        B_VEMPTY = B_VFULL + VST, B_SFULL = B_VEMPTY + VST,
-                       B_SFREE = B_SFULL + 1, B_DPFULL = B_SFULL + 2, B_PFULL = B_SFULL + 4,
-                       B_DONE = B_SFULL + 6, B_DRAIN = B_DONE + 1,
+                       B_SFREE = B_SFULL + 2, B_DPFULL = B_SFULL + 3, B_PFULL = B_SFULL + 5,
+                       B_DONE = B_SFULL + 7, B_DRAIN = B_DONE + 1,
                        B_CLCFULL = B_DRAIN + 1, B_CLCEMPTY = B_CLCFULL + kClcSlots,
                        NBAR = B_CLCEMPTY + kClcSlots;
   static constexpr int OFF_CLC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // item responses
@@ -598,30 +622,41 @@ struct DqCfg {
   static constexpr int THREADS = 128 + 128 * NWG;
   // Registers per thread after the warpgroup split (0: no split); the launch
   // must hold THREADS x launch registers >= REG_NEEDED (checked on the host).
-  static constexpr int REG_CTRL = 64, REG_SOFT = 104;
+  // Four softmax warpgroups (640 threads) get 104 registers each from the
+  // producer / MMA warpgroup's 64; with two (384 threads) every thread has
+  // enough at launch.
+  static constexpr int REG_CTRL = NWG == 4 ? 64 : 0, REG_SOFT = NWG == 4 ? 104 : 0;
   static constexpr int REG_NEEDED = REG_SOFT > 0 ? 128 * REG_CTRL + 128 * NWG * REG_SOFT : 0;
-  static constexpr int S_COL = 0;
-  static constexpr int DP_COL0 = 128;  // two dP blocks, 128 columns apart
-  static constexpr int DQ_COL = 384;   // one dQ accumulator
-  static constexpr uint32_t dp_col(int b) { return DP_COL0 + 128 * b; }
+  // TMEM. Q in shared memory: S at 0, dP blocks at BN and 2 BN (tile j uses
+  // dp block j % 2). Q in TMEM: blocks at 0 and BN, tile j uses block j % 2
+  // for S and then dP; Q (16-bit pairs, DP / 2 columns) after them.
+  static constexpr int QT_COL = 2 * BN;
+  static constexpr int DQ_COL = 512 - DP;  // one dQ accumulator
+  static constexpr uint32_t s_col(int b) { return QTM ? BN * b : 0; }
+  static constexpr uint32_t dp_col(int b) { return QTM ? BN * b : BN + BN * b; }
   static constexpr uint32_t ds_col(int b, int kk) { return chunk_operand_col(dp_col(b), kk); }
-  static_assert(NWG == 4, "one 32-column chunk per softmax warpgroup");
-  static_assert(D <= 128, "dQ accumulator in TMEM columns 384-511");
+  static_assert(CW == 32, "one 32-column chunk per softmax warpgroup");
+  static_assert((QTM ? 2 * BN + DP / 2 : 3 * BN) <= DQ_COL,
+                "score blocks, Q and dQ in 512 TMEM columns");
+  static_assert(!QTM || (DP / 2) % (32 * NWG) == 0, "Q columns split evenly over the warpgroups");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// Two dP blocks in TMEM and one dQ accumulator: dP(j+1) is computed while the
-// softmax still turns dP(j) into dS(j), so the tensor core runs S(j+1),
-// dP(j+1), dQ(j) without waiting for dQ(j) to read dS. The item's dQ store is
-// ordered before the next item's first dQ by the softmax warps' next dS
-// arrival (as in dK/dV). Persistent like the dK/dV kernel above.
+// Pipelined dQ. dP alternates between two TMEM blocks, so dP(j+1) is computed
+// while the softmax still turns dP(j) into dS(j), and the tensor core runs
+// S(j+1), dP(j+1), dQ(j) without waiting for dQ(j) to read dS. With Q in TMEM
+// the score of tile j+1 shares its block with dP(j+1): S(j+1) goes there after
+// dQ(j-1) has read the block (issue order), and dP(j+1) once the softmax has
+// read S(j+1). The item's dQ store is ordered before the next item's first dQ
+// by the softmax warps' next dS arrival (as in dK/dV). Persistent like the
+// dK/dV kernel above.
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
 fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-                 const float* __restrict__ lse, const float* __restrict__ dvec,
-                 void* __restrict__ dq_out, float scale, AttnShape s, TileOrder order,
-                 WaitCfg wc) {
+                 const void* __restrict__ q_rows, const float* __restrict__ lse,
+                 const float* __restrict__ dvec, void* __restrict__ dq_out, float scale,
+                 AttnShape s, TileOrder order, WaitCfg wc) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
@@ -642,6 +677,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       uint32_t cnt = 1;
       if (i == C::B_PFULL || i == C::B_PFULL + 1 || i == C::B_SFREE)
         cnt = 4 * C::NWG;  // one arrival per softmax warp
+      if (C::QTM && i == C::B_QFULL) cnt = 4 * C::NWG;
       if (i >= C::B_CLCEMPTY && i < C::B_CLCEMPTY + kClcSlots) cnt = C::THREADS / 32;
       mbar_init(bar(i), cnt);
     }
@@ -660,7 +696,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
   // producer / MMA warpgroup: registers handed to the softmax
   if constexpr (C::REG_SOFT > 0) regs_release<C::REG_CTRL>();
   if (warp == 3) {
-    // ------------------------------------------------ producer: Q and dO
+    // ------------------------------------------ producer: Q (unless in TMEM), dO
     // once per item, each as soon as the previous item's last MMA reading it
     // (its last S, its last dP) completes; read once, so not kept in L2
     const bool leader = elect_one_sync();
@@ -670,24 +706,26 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     for (int k = 0, item = blockIdx.x; ok; ++k) {
       const DqItem t = dq_item(item, order, s, C::BN);
       if (t.n_iter > 0) {
-        if (ln > 0) ok = mbar_wait(bar(C::B_QEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
-        if (!ok) break;
-        if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE);
-        for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d_hint(sbase + C::OFF_Q + r * C::REGION, &map_q, bar(C::B_QFULL), r * 64, t.q0, t.bh, pol_once);
-        ++nq;
+        if constexpr (!C::QTM) {
+          if (ln > 0) ok = mbar_wait(bar(C::B_QEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
+          if (!ok) break;
+          if (leader) mbar_arrive_expect_tx(bar(C::B_QFULL), C::Q_TILE);
+          for (int r = 0; r < C::KREG; ++r)
+            if (leader) tma_load_3d_hint(sbase + C::OFF_Q + r * C::Q_REGION, &map_q, bar(C::B_QFULL), r * 64, t.q0, t.bh, pol_once);
+          ++nq;
+        }
         if (ln > 0) ok = mbar_wait(bar(C::B_DOEMPTY), (ln - 1) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
-        if (leader) mbar_arrive_expect_tx(bar(C::B_DOFULL), C::TILE);
+        if (leader) mbar_arrive_expect_tx(bar(C::B_DOFULL), C::Q_TILE);
         for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d_hint(sbase + C::OFF_DO + r * C::REGION, &map_do, bar(C::B_DOFULL), r * 64, t.q0, t.bh, pol_once);
+          if (leader) tma_load_3d_hint(sbase + C::OFF_DO + r * C::Q_REGION, &map_do, bar(C::B_DOFULL), r * 64, t.q0, t.bh, pol_once);
         ++ndo;
         ++ln;
       }
       if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
     }
     if (*abort_flag) {
-      drain_ring(bar(C::B_QFULL), 1, nq, tmo, wc.status);
+      if (!C::QTM) drain_ring(bar(C::B_QFULL), 1, nq, tmo, wc.status);
       drain_ring(bar(C::B_DOFULL), 1, ndo, tmo, wc.status);
     }
   } else if (warp == 0 || warp == 2) {
@@ -719,9 +757,9 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         const int st = gt % nst;
         if (gt >= nst) ok = mbar_wait(bar(empty + st), ((gt / nst) - 1) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
-        if (leader) mbar_arrive_expect_tx(bar(full + st), C::TILE);
+        if (leader) mbar_arrive_expect_tx(bar(full + st), C::KV_TILE);
         for (int r = 0; r < C::KREG; ++r)
-          if (leader) tma_load_3d_hint(ring + st * C::TILE + r * C::REGION, map, bar(full + st), r * 64, kr, zkv, pol_ring);
+          if (leader) tma_load_3d_hint(ring + st * C::KV_TILE + r * C::KV_REGION, map, bar(full + st), r * 64, kr, zkv, pol_ring);
       }
       if (!ok) break;
       if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
@@ -736,16 +774,47 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     constexpr uint32_t ab = C::BF16 ? 1 : 0;
     constexpr uint32_t idesc_s = make_idesc_f16(kBM, C::BN, ab, 0, 0);
     constexpr uint32_t idesc_q = make_idesc_f16(kBM, C::D, ab, 0, 1);
+    // score block = A B^T, K = head dim: A (Q or dO) K-major from shared memory
     auto issue_score = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
       const uint64_t ad = make_sdesc(a_base, 16, 1024, 2), bd = make_sdesc(b_base, 16, 1024, 2);
 #pragma unroll
       for (int kk = 0; kk < C::D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * C::REGION + (kk & 3) * 32;
-        if (leader) mma_ss(tmem + col, ad + (off >> 4), bd + (off >> 4), idesc_s, kk > 0);
+        const uint32_t off_a = (kk >> 2) * C::Q_REGION + (kk & 3) * 32;
+        const uint32_t off_b = (kk >> 2) * C::KV_REGION + (kk & 3) * 32;
+        if (leader) mma_ss(tmem + col, ad + (off_a >> 4), bd + (off_b >> 4), idesc_s, kk > 0);
+      }
+    };
+    // S(gi) = Q K^T into its block, with Q from TMEM (QTM) or shared memory
+    auto issue_s = [&](int gi) {
+      const uint32_t k_base = sbase + C::OFF_K + (gi % C::KST) * C::KV_TILE;
+      if constexpr (C::QTM) {
+        const uint64_t bd = make_sdesc(k_base, 16, 1024, 2);
+#pragma unroll
+        for (int kk = 0; kk < C::D / 16; ++kk) {
+          const uint32_t off_b = (kk >> 2) * C::KV_REGION + (kk & 3) * 32;
+          if (leader) mma_ts(tmem + C::s_col(gi & 1), tmem + C::QT_COL + 8 * kk, bd + (off_b >> 4), idesc_s, kk > 0);
+        }
+      } else {
+        issue_score(sbase + C::OFF_Q, k_base, C::s_col(gi & 1));
       }
     };
     auto wait = [&](int b, int parity) {
       return mbar_wait_poll(bar(b), parity & 1, tmo, abort_flag, wc.status);
+    };
+    // dQ += dS K   (dS from TMEM, K as MN-major B, K = key rows)
+    auto issue_dq = [&](int gi, int it) {
+      const uint64_t kdesc = make_sdesc(sbase + C::OFF_K + (gi % C::KST) * C::KV_TILE, C::KV_REGION, 1024, 2);
+#pragma unroll
+      for (int kk = 0; kk < C::BN / 16; ++kk)
+        if (leader) mma_ts(tmem + C::DQ_COL, tmem + C::ds_col(gi & 1, kk), kdesc + ((kk * 16 * 128) >> 4), idesc_q,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+      if (leader) mma_commit(bar(C::B_KEMPTY + gi % C::KST));
+    };
+    // dP(gi) into its block; V is read by dP only
+    auto issue_dp = [&](int gi) {
+      issue_score(sbase + C::OFF_DO, sbase + C::OFF_V + (gi % C::VST) * C::KV_TILE, C::dp_col(gi & 1));
+      if (leader) mma_commit(bar(C::B_DPFULL + (gi & 1)));
+      if (leader) mma_commit(bar(C::B_VEMPTY + gi % C::VST));
     };
     int gt = 0, ln = 0;
     bool ok = true;
@@ -753,58 +822,63 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       const DqItem t = dq_item(item, order, s, C::BN);
       const int n = t.n_iter;
       if (n > 0) {
-        // S of the item's first tile: its Q, K(gt), and the softmax done
-        // reading the previous S
+        // S of the item's first tile: its Q, K(gt), and (Q in shared memory)
+        // the softmax done reading the previous S
         ok = wait(C::B_QFULL, ln) && wait(C::B_KFULL + gt % C::KST, gt / C::KST) &&
-             (gt == 0 || wait(C::B_SFREE, gt - 1));
+             (C::QTM || gt == 0 || wait(C::B_SFREE, gt - 1));
         if (!ok) break;
         tc_fence_after();
-        if (leader) issue_score(sbase + C::OFF_Q, sbase + C::OFF_K + (gt % C::KST) * C::TILE, C::S_COL);
-        if (leader) mma_commit(bar(C::B_SFULL));
-        if (n == 1 && leader) mma_commit(bar(C::B_QEMPTY));  // Q read for the last time
-        // dP of the first tile into block gt % 2 (its dS of two tiles back was
-        // read by a dQ issued before)
-        ok = wait(C::B_DOFULL, ln) && wait(C::B_VFULL + gt % C::VST, gt / C::VST);
+        issue_s(gt);
+        if (leader) mma_commit(bar(C::B_SFULL + (C::QTM ? (gt & 1) : 0)));
+        if (!C::QTM && n == 1 && leader) mma_commit(bar(C::B_QEMPTY));  // Q read for the last time
+        // dP of the first tile (its block's dS of the previous item was read
+        // by a dQ issued before; with Q in TMEM, once S(gt) was read from it)
+        ok = wait(C::B_DOFULL, ln) && wait(C::B_VFULL + gt % C::VST, gt / C::VST) &&
+             (!C::QTM || wait(C::B_SFREE, gt));
         if (!ok) break;
         tc_fence_after();
-        if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V + (gt % C::VST) * C::TILE, C::dp_col(gt & 1));
-        if (leader) mma_commit(bar(C::B_DPFULL + (gt & 1)));
-        if (leader) mma_commit(bar(C::B_VEMPTY + gt % C::VST));  // V is read by dP only
+        issue_dp(gt);
         if (n == 1 && leader) mma_commit(bar(C::B_DOEMPTY));
         for (int it = 0; it < n; ++it) {
           const int gi = gt + it;
-          const int ks = gi % C::KST;
           const bool more = it + 1 < n;
           if (more) {
+            // S(it+1): with Q in shared memory over the S block the softmax has
+            // read; with Q in TMEM into the block dQ(it-1) has read (issue order)
             const int nk = (gi + 1) % C::KST;
-            ok = wait(C::B_KFULL + nk, (gi + 1) / C::KST) && wait(C::B_SFREE, gi);
+            ok = wait(C::B_KFULL + nk, (gi + 1) / C::KST) && (C::QTM || wait(C::B_SFREE, gi));
             if (!ok) break;
             tc_fence_after();
-            if (leader) issue_score(sbase + C::OFF_Q, sbase + C::OFF_K + nk * C::TILE, C::S_COL);
-            if (leader) mma_commit(bar(C::B_SFULL));
-            if (it + 2 == n && leader) mma_commit(bar(C::B_QEMPTY));
-            // dP(it+1) into the other block (its dS(it-1) was read by dQ(it-1))
-            const int nv = (gi + 1) % C::VST;
-            ok = wait(C::B_VFULL + nv, (gi + 1) / C::VST);
-            if (!ok) break;
-            tc_fence_after();
-            if (leader) issue_score(sbase + C::OFF_DO, sbase + C::OFF_V + nv * C::TILE, C::dp_col((gi + 1) & 1));
-            if (leader) mma_commit(bar(C::B_DPFULL + ((gi + 1) & 1)));
-            if (leader) mma_commit(bar(C::B_VEMPTY + nv));
-            if (it + 2 == n && leader) mma_commit(bar(C::B_DOEMPTY));
+            issue_s(gi + 1);
+            if (leader) mma_commit(bar(C::B_SFULL + (C::QTM ? ((gi + 1) & 1) : 0)));
+            if (!C::QTM && it + 2 == n && leader) mma_commit(bar(C::B_QEMPTY));
+            if constexpr (!C::QTM) {
+              // dP(it+1) into the other block (its dS(it-1) was read by dQ(it-1))
+              const int nv = (gi + 1) % C::VST;
+              ok = wait(C::B_VFULL + nv, (gi + 1) / C::VST);
+              if (!ok) break;
+              tc_fence_after();
+              issue_dp(gi + 1);
+              if (it + 2 == n && leader) mma_commit(bar(C::B_DOEMPTY));
+            }
           }
           // dS(it) in TMEM; for the item's first tile this also means the
           // softmax warps have stored the previous item's dQ
           ok = wait(C::B_PFULL + (gi & 1), gi >> 1);
           if (!ok) break;
           tc_fence_after();
-          // dQ += dS K   (dS from TMEM, K as MN-major B, K = key rows)
-          const uint64_t kdesc = make_sdesc(sbase + C::OFF_K + ks * C::TILE, C::REGION, 1024, 2);
-#pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk)
-            if (leader) mma_ts(tmem + C::DQ_COL, tmem + C::ds_col(gi & 1, kk), kdesc + ((kk * 16 * 128) >> 4), idesc_q,
-                               (it > 0 || kk > 0) ? 1u : 0u);
-          if (leader) mma_commit(bar(C::B_KEMPTY + ks));
+          issue_dq(gi, it);
+          if (C::QTM && more) {
+            // dP(it+1) into S(it+1)'s block once the softmax has read S(it+1)
+            // (it does while dQ(it) runs); the issuing thread blocks while the
+            // tensor core works through a batch, so dQ(it) goes first
+            const int nv = (gi + 1) % C::VST;
+            ok = wait(C::B_VFULL + nv, (gi + 1) / C::VST) && wait(C::B_SFREE, gi + 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp(gi + 1);
+            if (it + 2 == n && leader) mma_commit(bar(C::B_DOEMPTY));
+          }
         }
         if (!ok) break;
         if (leader) mma_commit(bar(C::B_DONE));  // this item's dQ is final
@@ -823,7 +897,6 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint64_t c2 = f2_pack(s.scale_log2, s.scale_log2);
-    const uint32_t col0 = C::DP_COL0 + wg * C::CW;  // this warpgroup's chunk of dP block 0
     using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
     // LSE and D of this thread's row of an item (loaded one item ahead)
     auto row_stats = [&](const DqItem& u, float* L, float* dv) {
@@ -836,9 +909,37 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         *dv = dvec[idx];
       }
     };
+    // Q in TMEM: this warpgroup writes its share of the item's Q columns for
+    // its thread's row (zeros past Tq), then tells the MMA warp. Called once
+    // the previous item's last S has completed (the warps waited for it).
+    auto load_q_rows = [&](const DqItem& u) {
+      if constexpr (C::QTM) {
+        if (u.n_iter == 0) return;
+        constexpr int COLS = C::DP / 2 / C::NWG;   // 32-bit TMEM columns per warpgroup
+        const int r = u.q0 + quarter * 32 + lane;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const T16*>(q_rows) + (static_cast<int64_t>(u.bh) * s.Tq + (r < s.Tq ? r : 0)) * C::D) +
+            wg * (COLS / 4);
+#pragma unroll
+        for (int c = 0; c < COLS; c += 32) {
+          uint32_t w[32];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint4 x = r < s.Tq ? __ldg(src + c / 4 + e) : make_uint4(0, 0, 0, 0);
+            w[4 * e] = x.x; w[4 * e + 1] = x.y; w[4 * e + 2] = x.z; w[4 * e + 3] = x.w;
+          }
+          tmem_st32(tmem + lane_base + C::QT_COL + wg * COLS + c, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_QFULL));
+      }
+    };
     DqItem t = dq_item(blockIdx.x, order, s, C::BN);
     float L, dv;
     row_stats(t, &L, &dv);
+    load_q_rows(t);
     int gt = 0, ln = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -849,11 +950,13 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       for (int it = 0; it < t.n_iter; ++it) {
         const int gi = gt + it;
         const int kb = (t.j_lo + it) * C::BN + wg * C::CW;
-        ok = mbar_wait(bar(C::B_SFULL), gi & 1, tmo, abort_flag, wc.status);
+        // with Q in TMEM, S alternates between two blocks (and s_full barriers)
+        const int sb = C::QTM ? (gi & 1) : 0;
+        ok = mbar_wait(bar(C::B_SFULL + sb), (C::QTM ? (gi >> 1) : gi) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         tc_fence_after();
         uint32_t sv[32];
-        tmem_ld32(tmem + lane_base + C::S_COL + wg * C::CW, sv);
+        tmem_ld32(tmem + lane_base + C::s_col(gi & 1) + wg * C::CW, sv);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
@@ -869,7 +972,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
         ok = mbar_wait(bar(C::B_DPFULL + (gi & 1)), (gi >> 1) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t col = col0 + 128 * (gi & 1);
+        const uint32_t col = C::dp_col(gi & 1) + wg * C::CW;
         uint32_t pv[32];
         tmem_ld32(tmem + lane_base + col, pv);
         tmem_ld_wait();
@@ -898,18 +1001,19 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       if (more) {
         tn = dq_item(next, order, s, C::BN);
         row_stats(tn, &Ln, &dvn);
+        // this item's last S has completed (waited for above), so its Q
+        // columns are free for the next item's rows
+        load_q_rows(tn);
       }
       // ----------------------------------------------------- item epilogue
-      // 16-column chunks of the dQ row dealt round-robin over the softmax
-      // warpgroups; then the accumulator is free for the item after next
+      // 32-column blocks of the dQ rows dealt round-robin over the warps of
+      // this lane quarter; then the accumulator is free for the next item
       const bool have = t.n_iter > 0;
       if (have) {
         ok = mbar_wait(bar(C::B_DONE), ln & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         tc_fence_after();
       }
-      // 32-column blocks of the dQ rows dealt round-robin over the warps of
-      // this lane quarter
       const int row0 = t.q0 + quarter * 32;
       const int rows_valid = min(32, s.Tq - row0);
       T16* dst_blk = reinterpret_cast<T16*>(dq_out) +

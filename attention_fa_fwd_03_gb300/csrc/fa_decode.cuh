@@ -89,28 +89,6 @@ __device__ __forceinline__ uint32_t stage_offset(int region_bytes, int r, int d)
          static_cast<uint32_t>((d & 7) * 2);
 }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Split cluster barrier: every CTA of the cluster has started (its shared
-// memory may be written by peers) once the wait returns.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-}
-
-// Every thread of every CTA of the cluster arrives; release / acquire order
-// the shared-memory writes before the barrier with the peers' reads after it.
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Store v to CTA `rank`'s shared memory, at the offset `p` has in this CTA's.
 __device__ __forceinline__ void st_peer_f32(float* p, uint32_t rank, float v) {
   uint32_t remote, local = smem_u32(p);

@@ -8,6 +8,7 @@
 #include <type_traits>
 
 #include "fa_bwd.cuh"
+#include "fa_bwd_d256.cuh"
 #include "fa_bwd_pipelined.cuh"
 #include "fa_decode.cuh"
 #include "fa_fwd.cuh"
@@ -128,23 +129,24 @@ cudaError_t launch_dkv_with(const BwdLaunch& a, Kern kern) {
   return cudaGetLastError();
 }
 
-// The two D = 256 dK/dV passes as one grid (fa_bwd_dkv_split2_kernel).
-template <class CV, class CK>
-cudaError_t launch_dkv_split2(const BwdLaunch& a) {
-  const int bhq = a.s.B * a.s.Hq, bhkv = a.s.B * a.s.Hkv;
-  CUtensorMap mq, mk, mv, mdo;
-  if (!encode_tile_map(&mq, a.q, CV::BF16, CV::D, a.s.Tq, bhq, CV::BMQ) ||
-      !encode_tile_map(&mdo, a.dout, CV::BF16, CV::D, a.s.Tq, bhq, CV::BMQ) ||
-      !encode_tile_map(&mk, a.k, CV::BF16, CV::D, a.s.Tkv, bhkv, kBM) ||
-      !encode_tile_map(&mv, a.v, CV::BF16, CV::D, a.s.Tkv, bhkv, kBM))
+// D = 256 dK/dV: one cluster of two CTAs per 128-row KV block
+// (fa_bwd_dkv_pair_kernel), non-persistent, heaviest blocks first.
+template <class C>
+cudaError_t launch_dkv_pair(const BwdLaunch& a) {
+  const int bhq = a.s.B * a.s.Hq;
+  CUtensorMap mq, mdo;
+  if (!encode_tile_map(&mq, a.q, C::BF16, C::D, a.s.Tq, bhq, C::BMQ) ||
+      !encode_tile_map(&mdo, a.dout, C::BF16, C::D, a.s.Tq, bhq, C::BMQ))
     return cudaErrorInvalidValue;
-  auto kern = fa_bwd_dkv_split2_kernel<CV, CK>;
-  const int smem = CV::SMEM_BYTES > CK::SMEM_BYTES ? CV::SMEM_BYTES : CK::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = fa_bwd_dkv_pair_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const TileOrder order = kv_block_order(a.s, CV::D);
-  kern<<<2 * order.units * order.tiles, CV::THREADS, smem, a.stream>>>(
-      mq, mk, mv, mdo, a.lse, a.dvec, a.dk, a.dv, a.scale, a.s, order, a.wc);
+  const TileOrder order = kv_block_order(a.s, C::D);
+  const int64_t grid = int64_t(2) * order.units * order.tiles;
+  if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, a.stream>>>(
+      mq, mdo, a.k, a.v, a.lse, a.dvec, a.dk, a.dv, a.scale, a.s, order, a.wc);
   return cudaGetLastError();
 }
 
@@ -164,7 +166,7 @@ cudaError_t launch_dq_with(const BwdLaunch& a, Kern kern) {
     return cudaErrorInvalidConfiguration;
   const TileOrder order = query_block_order(a.s, kBM, C::D);
   kern<<<order.units * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream>>>(
-      mq, mk, mv, mdo, a.lse, a.dvec, a.dq, a.scale, a.s, order, a.wc);
+      mq, mk, mv, mdo, a.q, a.lse, a.dvec, a.dq, a.scale, a.s, order, a.wc);
   return cudaGetLastError();
 }
 
@@ -174,9 +176,10 @@ cudaError_t launch_dq_with(const BwdLaunch& a, Kern kern) {
 constexpr int kSoftmaxWarpgroups = 4;
 
 // Backward for one head dim. D <= 128: the pipelined 128 x 128 kernels
-// (fa_bwd_pipelined.cuh). D = 256: the accumulators alone fill TMEM, so dV and
-// dK run as two passes with 64-row query tiles and dQ with 64-column key
-// tiles, one stage (fa_bwd.cuh).
+// (fa_bwd_pipelined.cuh). D = 256: the dK and dV accumulators alone fill TMEM,
+// so dV and dK are computed by the two CTAs of a cluster that exchange P
+// (fa_bwd_d256.cuh), and dQ runs the pipelined kernel with 64-key tiles and Q
+// in TMEM.
 // dQ of short query blocks on the split-key kernel (defined below)
 template <int D, bool BF16>
 cudaError_t run_dq_decode(const BwdLaunch& a);
@@ -191,9 +194,7 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
       using C = DkvCfg<D, BF16, kSoftmaxWarpgroups>;
       e = launch_dkv_with<C>(a, fa_bwd_dkv_kernel<C>);
     } else {
-      using CV = DkvSplitCfg<D, 64, 2, BF16, kModeDV>;
-      using CK = DkvSplitCfg<D, 64, 1, BF16, kModeDK>;
-      e = launch_dkv_split2<CV, CK>(a);
+      e = launch_dkv_pair<DkvPairCfg<BF16>>(a);
     }
   }
   if (e != cudaSuccess) return e;
@@ -203,8 +204,9 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
       using C = DqCfg<D, BF16, kSoftmaxWarpgroups>;
       e = launch_dq_with<C>(a, fa_bwd_dq_kernel<C>);
     } else {
-      using C = DqSerialCfg<D, 64, 1, BF16>;
-      e = launch_dq_with<C>(a, fa_bwd_dq_serial_kernel<C>);
+      // 64-key tiles, two softmax warpgroups, Q in TMEM, K / V rings 3 / 2
+      using C = DqCfg<D, BF16, 2, 64, 3, 2, true>;
+      e = launch_dq_with<C>(a, fa_bwd_dq_kernel<C>);
     }
   }
   return e;

@@ -106,8 +106,9 @@ KERNEL_SOURCES = {
     "fa_fwd_decode_kernel": ["fa_decode.cuh"],
     "fa_bwd_dq_decode_kernel": ["fa_decode.cuh"],
     "fa_bwd_dvec_kernel": ["fa_bwd.cuh"],
-    "fa_bwd_dkv_kernel": ["fa_bwd_pipelined.cuh", "fa_bwd.cuh"],
-    "fa_bwd_dq_kernel": ["fa_bwd_pipelined.cuh", "fa_bwd.cuh"],
+    "fa_bwd_dkv_kernel": ["fa_bwd_pipelined.cuh"],
+    "fa_bwd_dkv_pair_kernel": ["fa_bwd_d256.cuh", "fa_bwd_pipelined.cuh"],
+    "fa_bwd_dq_kernel": ["fa_bwd_pipelined.cuh"],
 }
 COMMON_SOURCES = ["fa_common.cuh", "sm103_ptx.cuh", "fa_inst.cuh", "fa_inst_d64.cu",
                   "fa_inst_d96.cu", "fa_inst_d128.cu", "fa_inst_d256.cu"]
@@ -306,7 +307,7 @@ def run_ours(args, rank, world, local_rank):
     ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.Hq, w.Tq), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sc, ca, wi = w.scale, w.causal, w.window
-    n_dkv = 1  # one dK/dV launch per step (at D = 256 both passes share one grid)
+    n_dkv = 1  # one dK/dV launch per step
 
     def step(ev):
         ev[0].record()
@@ -432,8 +433,10 @@ def run_ours(args, rank, world, local_rank):
     # query blocks of at most 8 rows per head run the split-key CUDA-core
     # forward and dQ kernels (latency- and HBM-bound: reported against HBM)
     short = w.Tq <= 8
+    # head dim 256: dK/dV on two-CTA clusters
     names = ["fa_fwd_decode_kernel" if short else "fa_fwd_kernel", "fa_bwd_dvec_kernel",
-             "fa_bwd_dkv_kernel", "fa_bwd_dq_decode_kernel" if short else "fa_bwd_dq_kernel"]
+             "fa_bwd_dkv_pair_kernel" if w.D == 256 else "fa_bwd_dkv_kernel",
+             "fa_bwd_dq_decode_kernel" if short else "fa_bwd_dq_kernel"]
     avg_ms = [sum(p) / len(p) for p in phase_ms]
     # algorithmic work per launch: tensor FLOPs of each kernel's contractions over
     # the visible pairs (2*D per pair per contraction); bytes for the D-vector
@@ -445,6 +448,7 @@ def run_ours(args, rank, world, local_rank):
            "fa_fwd_decode_kernel": ("hbm", kv_bytes + 2 * row_bytes + w.B * w.Hq * w.Tq * 4),
            "fa_bwd_dvec_kernel": ("hbm", 2 * w.B * w.Hq * w.Tq * w.D * 2 + w.B * w.Hq * w.Tq * 4),
            "fa_bwd_dkv_kernel": ("tensor", 4 * 2 * w.D * pairs),
+           "fa_bwd_dkv_pair_kernel": ("tensor", 4 * 2 * w.D * pairs),
            "fa_bwd_dq_kernel": ("tensor", 3 * 2 * w.D * pairs),
            "fa_bwd_dq_decode_kernel": ("hbm", kv_bytes + 3 * row_bytes + 2 * w.B * w.Hq * w.Tq * 4)}
     kernels = {}
@@ -456,8 +460,7 @@ def run_ours(args, rank, world, local_rank):
             kernels[nm] = {"ms": round(ms, 4), "gbs": round(work / (ms / 1e3) / 1e9, 1)}
     dom = names[max(range(4), key=lambda j: avg_ms[j])]
     bound, work = alg[dom]
-    # the dK/dV phase is two launches at D=256 (dV pass, dK pass): per launch
-    launches = n_dkv if dom == "fa_bwd_dkv_kernel" else 1
+    launches = n_dkv if dom in ("fa_bwd_dkv_kernel", "fa_bwd_dkv_pair_kernel") else 1
     launch_s = avg_ms[names.index(dom)] / launches / 1e3
     work_per_launch = work / launches
     region_s = sum(step_ms) / 1e3
