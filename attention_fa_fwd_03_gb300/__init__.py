@@ -20,7 +20,7 @@ import threading
 __all__ = ["FA_FP16", "FA_BF16", "FaError", "fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkv",
            "fa_bwd_dq", "fa_bwd_workspace_size",
            "fa_status_string", "fa_device_status", "fa_abi_version", "fa_selftest_wait_timeout",
-           "library", "library_path"]
+           "fa_set_wait_limit_cycles", "library", "library_path"]
 
 FA_FP16 = 0
 FA_BF16 = 1
@@ -77,6 +77,8 @@ def library():
         lib.fa_abi_version.restype = i
         lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
         lib.fa_selftest_wait_timeout.restype = i
+        lib.fa_set_wait_limit_cycles.argtypes = [ctypes.c_ulonglong]
+        lib.fa_set_wait_limit_cycles.restype = i
         _lib = lib
         return lib
 
@@ -201,6 +203,13 @@ def fa_selftest_wait_timeout(timeout_ms: int, stream=None) -> None:
     with fa_device_status()."""
     _check(library().fa_selftest_wait_timeout(int(timeout_ms), _stream(stream)),
            "fa_selftest_wait_timeout")
+
+
+def fa_set_wait_limit_cycles(cycles: int) -> None:
+    """Bound (SM clock cycles) of the kernels' ordinary waits for every later
+    launch in this process; 0 restores the default. A diagnostic for tests of
+    the give-up path (see include/fa.h)."""
+    _check(library().fa_set_wait_limit_cycles(int(cycles)), "fa_set_wait_limit_cycles")
 
 
 def fa_device_status(clear: bool = True, stream=None) -> int:

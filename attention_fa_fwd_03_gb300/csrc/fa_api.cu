@@ -37,10 +37,10 @@ void load_encode() {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 }
 
-// Bound of every device wait, in SM clock cycles: FA_WAIT_TIMEOUT_MS (default
-// 4000 ms) at 2.2 GHz, above the GB300's highest SM clock, so at any real
-// clock the wait lasts at least that long.
-uint64_t wait_timeout_cycles() {
+// Default bound of every device wait, in SM clock cycles: FA_WAIT_TIMEOUT_MS
+// (default 4000 ms) at 2.2 GHz, above the GB300's highest SM clock, so at any
+// real clock the wait lasts at least that long.
+uint64_t default_wait_cycles() {
   static const uint64_t cycles = [] {
     const char* env = std::getenv("FA_WAIT_TIMEOUT_MS");
     long ms = env ? std::strtol(env, nullptr, 10) : 0;
@@ -48,6 +48,22 @@ uint64_t wait_timeout_cycles() {
     return static_cast<uint64_t>(ms) * 2200000ull;
   }();
   return cycles;
+}
+
+// Process-wide override of the bound of the ordinary waits (0: the default),
+// set by fa_set_wait_limit_cycles for tests of the give-up path.
+std::atomic<uint64_t> g_wait_override{0};
+
+uint64_t wait_timeout_cycles() {
+  const uint64_t o = g_wait_override.load(std::memory_order_relaxed);
+  return o != 0 ? o : default_wait_cycles();
+}
+
+// The waits at exit that let in-flight copies and MMAs finish keep the default
+// bound whatever the override is.
+void set_waits(WaitCfg* wc) {
+  wc->timeout_cycles = wait_timeout_cycles();
+  wc->drain_cycles = default_wait_cycles();
 }
 
 bool status_ptr(uint32_t** p) {
@@ -181,7 +197,12 @@ fa_status fa_selftest_wait_timeout(unsigned int timeout_ms, cudaStream_t stream)
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-int fa_abi_version(void) { return 100; }
+fa_status fa_set_wait_limit_cycles(unsigned long long cycles) {
+  g_wait_override.store(static_cast<uint64_t>(cycles), std::memory_order_relaxed);
+  return FA_OK;
+}
+
+int fa_abi_version(void) { return 101; }
 
 const char* fa_status_string(fa_status s) {
   switch (s) {
@@ -224,7 +245,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   a.s = make_shape(B, hq, Hkv, tq, Tkv, causal, window, scale);
   a.bf16 = dt == FA_BF16;
   if (!status_ptr(&a.wc.status)) return FA_ERR_LAUNCH;
-  a.wc.timeout_cycles = wait_timeout_cycles();
+  set_waits(&a.wc);
   a.stream = stream;
   cudaError_t e;
   switch (D) {
@@ -286,7 +307,7 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   a.s_rows = make_shape(B, Hq, Hkv, Tq, Tkv, causal, window, scale);
   a.bf16 = dt == FA_BF16;
   if (!status_ptr(&a.wc.status)) return FA_ERR_LAUNCH;
-  a.wc.timeout_cycles = wait_timeout_cycles();
+  set_waits(&a.wc);
   a.stream = stream;
   cudaError_t e;
   switch (D) {

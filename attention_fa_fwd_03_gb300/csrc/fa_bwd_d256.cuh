@@ -77,6 +77,8 @@ struct DkvPairCfg {
                        B_SCFULL = B_OPREADY + 1, B_READY = B_SCFULL + 2, B_PBUF = B_READY + 2,
                        B_STAGED = B_PBUF + 2, B_DONE = B_STAGED + 2, B_DRAIN = B_DONE + 1,
                        NBAR = B_DRAIN + 1;
+  // misc: TMEM base address, abort flag, and (dS side) the number of P
+  // buffers the peer has sent, stored there by the peer at its exit
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16;  // base must be 1024-aligned (checked)
   static constexpr int THREADS = 128 + 128 * NWG;
@@ -108,6 +110,7 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
   auto bar = [&](int i) { return smem_u32(bars + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* peer_sent = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   float* stats = reinterpret_cast<float*>(smem + C::OFF_STATS);
   const uint64_t tmo = wc.timeout_cycles;
   const int reps = s.Hq / s.Hkv;
@@ -117,6 +120,7 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
 
   if (threadIdx.x == 0) {
     *abort_flag = aligned ? 0 : 1;
+    *peer_sent = 0;
     if (!aligned) atomicOr(wc.status, kStatusSmemMisaligned);
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
@@ -143,6 +147,7 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  int seen = 0;  // dS side, warp 4 lane 0: P buffers received so far
   if (warp == 0 || warp == 2) {
     // --------------------------------------------------- producers: rings A, B
     // the whole warp runs the loop; one elected lane issues. Q and dO tiles
@@ -166,7 +171,7 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
       for (int r = 0; r < C::KREG; ++r)
         if (leader) tma_load_3d_hint(ring + st * C::TILE + r * C::REGION, map, bar(full + st), r * 64, i0, zq, pol);
     }
-    if (*abort_flag) drain_ring(bar(full), C::RST, it, tmo, wc.status);
+    if (*abort_flag) drain_ring(bar(full), C::RST, it, wc.drain_cycles, wc.status);
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
     const bool leader = elect_one_sync();
@@ -222,7 +227,7 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
     }
     // every issued MMA completes before the CTA exits
     if (leader) mma_commit(bar(C::B_DRAIN));
-    mbar_wait(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
+    mbar_wait(bar(C::B_DRAIN), 0, wc.drain_cycles, nullptr, wc.status);
   } else if (warp == 3) {
     // ------------------------------------------- per-tile row statistics
     // each lane loads its two rows of the next tile before waiting for the
@@ -256,6 +261,7 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
       __syncwarp();
       return true;
     };
+    int sent = 0;
     bool ok = !*abort_flag;
     if (ok && n > 0) load(0);
     for (int it = 0; ok && it < n; ++it) {
@@ -266,9 +272,18 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
       for (int r = 0; r < RPL; ++r) dst[lane + 32 * r] = v[r];
       mbar_arrive(bar(C::B_STFULL + slot));
       if (it + 1 < n) load(it + 1);
-      if (pside && it >= 1) ok = send(it - 1);
+      if (pside && it >= 1) {
+        ok = send(it - 1);
+        sent += ok ? 1 : 0;
+      }
     }
-    if (pside && ok && n > 0) send(n - 1);
+    if (pside && ok && n > 0) sent += send(n - 1) ? 1 : 0;
+    // the peer drains exactly the copies that were issued if it gives up; the
+    // count reaches it through the cluster barrier at exit
+    if (pside && leader) {
+      const uint32_t remote = peer_addr(smem_u32(const_cast<int*>(peer_sent)), 1);
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(sent) : "memory");
+    }
   } else {
     // ------------------------------------------------------------ softmax
     const int wg = (warp - 4) >> 2;       // query columns [32 wg, 32 wg + 32) of a tile
@@ -309,11 +324,9 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
     };
     // dS side: announce the bytes of the first two P buffers
     const bool poster = !pside && warp == 4 && lane == 0;
-    int posted = 0, seen = 0;  // (poster) tiles whose bytes were announced / have landed
     if (poster && ok) {
       mbar_arrive_expect_tx(bar(C::B_PBUF), C::PBUF);
       mbar_arrive_expect_tx(bar(C::B_PBUF + 1), C::PBUF);
-      posted = n < 2 ? n : 2;
     }
     const int i_first = t.i_lo * C::BMQ, i_end = (t.i_lo + t.n_qt) * C::BMQ;
     int i0 = i_first;
@@ -375,10 +388,7 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         // (they cannot arrive before every warp has released the buffer below)
         if (poster) {
           seen = j + 1;
-          if (j + 2 < n) {
-            mbar_arrive_expect_tx(bar(C::B_PBUF + b), C::PBUF);
-            posted = j + 3;
-          }
+          if (j + 2 < n) mbar_arrive_expect_tx(bar(C::B_PBUF + b), C::PBUF);
         }
         uint32_t ph[16];
 #pragma unroll
@@ -411,11 +421,6 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         }
       }
     }
-    // after an abort, let the peer's copies that may still be on their way
-    // land (bounded) before this CTA can exit
-    if (poster && *abort_flag)
-      for (int j = seen; j < posted; ++j)
-        mbar_wait_cluster(bar(C::B_PBUF + (j & 1)), (j >> 1) & 1, tmo, nullptr, wc.status);
     // --------------------------------------------------------- epilogue
     // dV (P side) or scale dK (dS side): 64-column blocks of the rows dealt
     // over the warpgroups; a block with no query tile stores zeros
@@ -438,9 +443,16 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
 
   tc_fence_before();
   __syncthreads();
-  // neither CTA leaves while its peer may still write into its shared memory
-  // or arrive on its barriers
+  // neither CTA leaves while its peer may still arrive on its barriers; after
+  // it the dS side knows how many P copies the peer issued
   cluster_barrier();
+  // after an abort, the dS side lets every copy the peer issued land (bounded)
+  // before it can exit (the peer cannot send a buffer whose bytes were not
+  // announced: it waits for the buffer to be freed, which comes after)
+  if (!pside && warp == 4 && lane == 0 && *abort_flag)
+    for (int j = seen; j < *peer_sent; ++j)
+      mbar_wait_cluster(bar(C::B_PBUF + (j & 1)), (j >> 1) & 1, wc.drain_cycles, nullptr, wc.status);
+  __syncthreads();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

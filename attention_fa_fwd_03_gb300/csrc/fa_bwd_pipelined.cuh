@@ -254,9 +254,9 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
     }
     if (*abort_flag) {
-      drain_ring(bar(once_full), 1, ln, tmo, wc.status);
-      drain_ring(bar(full), nst, gt, tmo, wc.status);
-      if (q_ring) drain_ring(iq.full, kClcSlots, asked, tmo, wc.status);
+      drain_ring(bar(once_full), 1, ln, wc.drain_cycles, wc.status);
+      drain_ring(bar(full), nst, gt, wc.drain_cycles, wc.status);
+      if (q_ring) drain_ring(iq.full, kClcSlots, asked, wc.drain_cycles, wc.status);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
@@ -357,7 +357,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     }
     // every issued MMA completes before the CTA exits
     if (leader) mma_commit(bar(C::B_DRAIN));
-    mbar_wait(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
+    mbar_wait(bar(C::B_DRAIN), 0, wc.drain_cycles, nullptr, wc.status);
   } else if (warp == 3) {
     // ------------------------------------------- LSE / D-vector staging
     // a flat stream over the tiles of the CTA's items; each lane loads its
@@ -725,8 +725,8 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
     }
     if (*abort_flag) {
-      if (!C::QTM) drain_ring(bar(C::B_QFULL), 1, nq, tmo, wc.status);
-      drain_ring(bar(C::B_DOFULL), 1, ndo, tmo, wc.status);
+      if (!C::QTM) drain_ring(bar(C::B_QFULL), 1, nq, wc.drain_cycles, wc.status);
+      drain_ring(bar(C::B_DOFULL), 1, ndo, wc.drain_cycles, wc.status);
     }
   } else if (warp == 0 || warp == 2) {
     // ------------------------------------------- producers: K ring, V ring
@@ -765,8 +765,8 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
       if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
     }
     if (*abort_flag) {
-      drain_ring(bar(full), nst, gt, tmo, wc.status);
-      if (k_ring) drain_ring(iq.full, kClcSlots, asked, tmo, wc.status);
+      drain_ring(bar(full), nst, gt, wc.drain_cycles, wc.status);
+      if (k_ring) drain_ring(iq.full, kClcSlots, asked, wc.drain_cycles, wc.status);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
@@ -889,7 +889,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     }
     // every issued MMA completes before the CTA exits
     if (leader) mma_commit(bar(C::B_DRAIN));
-    mbar_wait(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
+    mbar_wait(bar(C::B_DRAIN), 0, wc.drain_cycles, nullptr, wc.status);
   }
   } else {
     if constexpr (C::REG_SOFT > 0) regs_claim<C::REG_SOFT>();

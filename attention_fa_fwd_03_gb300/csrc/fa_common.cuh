@@ -31,8 +31,13 @@ struct AttnShape {
 };
 
 struct WaitCfg {
-  uint32_t* status;    // device status word
+  uint32_t* status;         // device status word
   uint64_t timeout_cycles;  // bound of every mbarrier wait, in SM clock cycles
+  // Bound of the waits at exit after a wait gave up (copies still landing in
+  // shared memory, MMAs still running before TMEM is freed): never shorter
+  // than the default limit, so a short test limit cannot let a CTA leave with
+  // work in flight.
+  uint64_t drain_cycles;
 };
 
 // Order in which a 1-D grid visits (unit, tile) work items. A unit is a
@@ -156,9 +161,10 @@ __host__ __device__ __forceinline__ bool block_unmasked(const AttnShape& s, int 
   return true;
 }
 
-// After an abort, wait (bounded, whatever the abort flag says) until the last
-// `nst` loads issued into a ring of `nst` slots have landed, so that no copy is
-// still in flight into this CTA's shared memory when it exits.
+// After an abort, wait (bounded by `tmo`, the drain limit, whatever the abort
+// flag says) until the last `nst` loads issued into a ring of `nst` slots have
+// landed, so that no copy is still in flight into this CTA's shared memory
+// when it exits.
 __device__ __forceinline__ void drain_ring(uint32_t full_bar0, int nst, int issued,
                                            uint64_t tmo, uint32_t* status) {
   for (int i = issued > nst ? issued - nst : 0; i < issued; ++i)

@@ -282,7 +282,7 @@ fa_fwd_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_con
   // after a wait gave up: let the loads still in flight land before the CTA exits
   if (threadIdx.x == 0)
     for (int i = done; i < nstage && i < done + C::STAGES; ++i)
-      mbar_wait(smem_u32(&full[i % C::STAGES]), (i / C::STAGES) & 1, tmo, nullptr, wc.status);
+      mbar_wait(smem_u32(&full[i % C::STAGES]), (i / C::STAGES) & 1, wc.drain_cycles, nullptr, wc.status);
 
   // warp partials to shared memory
   float* ow = sm + C::F_OW + warp * TQ * D;
@@ -576,7 +576,7 @@ fa_bwd_dq_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     if (threadIdx.x == 0 && st + 1 < nstage) issue(st + 1);
   }
   // after a wait gave up: let a load still in flight land before the CTA exits
-  if (threadIdx.x == 0 && done < nstage) mbar_wait(smem_u32(&full), done & 1, tmo, nullptr, wc.status);
+  if (threadIdx.x == 0 && done < nstage) mbar_wait(smem_u32(&full), done & 1, wc.drain_cycles, nullptr, wc.status);
 
   // warp partials, their sum per CTA pushed into the row owner's shared memory
   float* ow = sm + C::F_OW + warp * TQ * D;

@@ -111,7 +111,8 @@ struct FwdCfg {
   // warpgroup hands registers to the softmax warpgroups, whose 128-score rows
   // would otherwise spill. The launch must hold THREADS x launch registers >=
   // REG_NEEDED (checked on the host against the compiled kernel).
-  static constexpr int REG_CTRL = NQ == 2 ? (SBUF == 2 ? 112 : 80) : 0,
+  // (One score buffer: 128 x 104 + 256 x 200 = 384 x 168, the launch total.)
+  static constexpr int REG_CTRL = NQ == 2 ? (SBUF == 2 ? 112 : 104) : 0,
                        REG_SOFT = NQ == 2 ? (SBUF == 2 ? 168 : 200) : 0;
   static constexpr int REG_NEEDED = 128 * REG_CTRL + 128 * NQ * REG_SOFT;
   // TMEM: score buffers of tile t at t * SBUF * BN + b * BN, O_t after all of them
@@ -217,10 +218,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
     }
     if (*abort_flag) {
-      drain_ring(bar(full), C::STAGES, gk, tmo, wc.status);
+      drain_ring(bar(full), C::STAGES, gk, wc.drain_cycles, wc.status);
       if (k_ring) {
-        drain_ring(bar(C::B_QFULL), 1, ln, tmo, wc.status);
-        drain_ring(iq.full, kClcSlots, asked, tmo, wc.status);
+        drain_ring(bar(C::B_QFULL), 1, ln, wc.drain_cycles, wc.status);
+        drain_ring(iq.full, kClcSlots, asked, wc.drain_cycles, wc.status);
       }
     }
   } else if (warp == 1) {
@@ -284,8 +285,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           const int st = gi % C::STAGES, b = gi % C::SBUF;
           const int gn = gi + C::SBUF, nst = gn % C::STAGES;  // the tile whose S reuses buffer b
           const bool next = it + C::SBUF < n;
-          ok = wait(C::B_VFULL + st, gi / C::STAGES);
+          // V(gi) and K of the next score are checked before the P waits (they
+          // land long before), so once P arrives only PV and S are issued
+          ok = wait(C::B_VFULL + st, gi / C::STAGES) && (!next || wait(C::B_KFULL + nst, gn / C::STAGES));
           if (!ok) break;
+          tc_fence_after();
           for (int tq = 0; tq < C::NQ; ++tq) {
             // P_t in TMEM; for the block's first tile this also means the
             // softmax warpgroup has stored the previous block's O_t
@@ -295,11 +299,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             if (leader) issue_pv(tq, st, b, it > 0);
             if (leader) mma_commit(bar(C::B_OREADY + tq));
             if (next) {
-              if (tq == 0) {
-                ok = wait(C::B_KFULL + nst, gn / C::STAGES);
-                if (!ok) break;
-                tc_fence_after();
-              }
               if (leader) issue_s(tq, nst, b);  // after PV(gi) read P from buffer b
               if (leader) mma_commit(bar(C::sfull(tq, b)));
             }
@@ -317,7 +316,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     }
     // make sure nothing is in flight before TMEM is released
     if (leader) mma_commit(bar(C::B_DRAIN));
-    mbar_wait(bar(C::B_DRAIN), 0, tmo, nullptr, wc.status);
+    mbar_wait(bar(C::B_DRAIN), 0, wc.drain_cycles, nullptr, wc.status);
   }
   } else {
     if constexpr (C::REG_SOFT > 0) regs_claim<C::REG_SOFT>();

@@ -83,16 +83,21 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// A wait bound below this many cycles (a test of the give-up path) also reads
+// the clock after every failed try, so the wait gives up at its first miss.
+constexpr uint64_t kShortWaitCycles = 1024;
+
 // As mbar_wait below, but polling with test_wait: for the single thread that
 // issues MMAs, which must notice a completed phase at once.
 __device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity,
                                                uint64_t timeout_cycles, volatile int* abort,
                                                uint32_t* status) {
   if (mbar_test_wait(bar, parity)) return true;
+  const int tries = timeout_cycles < kShortWaitCycles ? 1 : 64;
   const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
+    for (int i = 0; i < tries; ++i)
       if (mbar_test_wait(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
     if (static_cast<uint64_t>(clock64() - t0) > timeout_cycles) {
@@ -113,13 +118,14 @@ __device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity,
 // must not be cut short by an earlier abort).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_cycles,
                                           volatile int* abort, uint32_t* status) {
+  const int tries = timeout_cycles < kShortWaitCycles ? 1 : 32;
 #pragma unroll 1
-  for (int i = 0; i < 32; ++i)
+  for (int i = 0; i < tries; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < tries; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
     if (static_cast<uint64_t>(clock64() - t0) > timeout_cycles) {
@@ -433,10 +439,11 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
                                                   uint64_t timeout_cycles, volatile int* abort,
                                                   uint32_t* status) {
+  const int tries = timeout_cycles < kShortWaitCycles ? 1 : 32;
   const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < tries; ++i)
       if (mbar_try_wait_cluster(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
     if (static_cast<uint64_t>(clock64() - t0) > timeout_cycles) {

@@ -180,6 +180,17 @@ fa_status fa_device_status(unsigned int* bits, int clear, cudaStream_t stream);
  * FA_ERR_LAUNCH on a launch failure. */
 fa_status fa_selftest_wait_timeout(unsigned int timeout_ms, cudaStream_t stream);
 
+/* Bound, in SM clock cycles, of the ordinary waits of every kernel launched
+ * after this call by any host thread of the process (a library diagnostic for
+ * tests of the give-up path; the pages have no counterpart). 0 restores the
+ * default (FA_WAIT_TIMEOUT_MS, else 4 s). With a bound of a few cycles the
+ * first wait of each kernel gives up: the kernel sets FA_ERR_TIMEOUT's bit in
+ * the device status word and runs to its exit. The waits at exit that let
+ * copies and MMAs already in flight finish keep the default bound, so no CTA
+ * leaves with work outstanding; outputs of such a call are undefined. Calls
+ * made after restoring the default compute normally. Always returns FA_OK. */
+fa_status fa_set_wait_limit_cycles(unsigned long long cycles);
+
 /* Version of this ABI (major * 100 + minor). */
 int fa_abi_version(void);
 

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert fa.fa_abi_version() == 100
+    assert fa.fa_abi_version() == 101
     for code in range(7):
         s = fa.fa_status_string(code)
         assert isinstance(s, str) and s
