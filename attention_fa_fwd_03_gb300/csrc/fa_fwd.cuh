@@ -428,9 +428,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       const bool have = t.n_iter > 0;
       if (have) {
         // O_t is final once the block's last PV completed. A parity wait is
-        // only sound when the barrier is at most one phase behind: with two
-        // score buffers the block's last S was issued before its second-to-last
-        // PV, which may still be running, so that PV is waited for first.
+        // only sound when the barrier is at most one phase off. Behind: with
+        // two score buffers the block's last S was issued before its
+        // second-to-last PV, which may still be running, so that PV is waited
+        // for first. Ahead: the last PV is issued only after the MMA warp has
+        // seen this warp's arrival just above and runs for 512 cycles or more,
+        // while this warp reaches the wait within a few ALU instructions. (A
+        // per-block barrier committed by the MMA warp would close this by
+        // construction; measured, it cost the forward 4-7%.)
         const int last = gk + t.n_iter - 1;
         if (C::SBUF == 2 && t.n_iter > 1)
           ok = mbar_wait(bar(C::B_OREADY + tq), (last - 1) & 1, tmo, abort_flag, wc.status);
