@@ -346,14 +346,30 @@ cudaError_t run_fwd_decode(const FwdLaunch& a) {
 
 }  // namespace fa
 
+// A forward grid of two-tile (256-row) query blocks that would leave SMs
+// idle: run one 128-row tile per CTA instead (twice the blocks; with one tile
+// a CTA's TMEM has room for two score buffers, so S(j+1) is computed while the
+// softmax works on S(j)).
+namespace fa {
+inline bool fwd_small_grid(const AttnShape& s) {
+  return static_cast<int64_t>(s.B) * s.Hq * ((s.Tq + 2 * kBM - 1) / (2 * kBM)) < device_sm_count();
+}
+}  // namespace fa
+
 // Define launch_fwd_d<D> / launch_bwd_d<D> for one head dim, given the forward
 // tile configuration (NQ query tiles per CTA, key tile BN, STAGES of the K/V
-// ring).
+// ring). With two query tiles per CTA, small grids take one tile per CTA and a
+// K/V ring three deep.
 #define FA_DEFINE_HEAD_DIM(D, FNQ, FBN, FST)                                              \
   namespace fa {                                                                          \
   cudaError_t launch_fwd_d##D(const FwdLaunch& a) {                                       \
     if (a.s.Tq <= kDecodeMaxTq)                                                           \
       return a.bf16 ? run_fwd_decode<D, true>(a) : run_fwd_decode<D, false>(a);           \
+    if constexpr (FNQ == 2) {                                                             \
+      if (fwd_small_grid(a.s))                                                            \
+        return a.bf16 ? run_fwd<FwdCfg<D, 1, FBN, 3, true>>(a)                            \
+                      : run_fwd<FwdCfg<D, 1, FBN, 3, false>>(a);                          \
+    }                                                                                     \
     return a.bf16 ? run_fwd<FwdCfg<D, FNQ, FBN, FST, true>>(a)                            \
                   : run_fwd<FwdCfg<D, FNQ, FBN, FST, false>>(a);                          \
   }                                                                                       \

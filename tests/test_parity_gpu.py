@@ -245,6 +245,9 @@ EDGE = [
     (1, 2, 1, 1, 1, 64, "fp16", False, 0),           # single key and query
     (1, 2, 2, 5, 700, 256, "bf16", False, 0),        # short queries, D=256
     (3, 6, 3, 256, 384, 96, "fp16", False, 0),       # exact tile multiples, cross-attention
+    # grids large enough for two 128-row query tiles per forward CTA, ragged tails
+    (4, 40, 8, 300, 300, 128, "bf16", True, 0),
+    (2, 80, 10, 200, 260, 64, "fp16", False, 70),
     # short query blocks (Tq <= 8): the split-key forward
     (1, 4, 2, 6, 300, 128, "bf16", True, 0),         # causal, top-left: row i sees i + 1 keys
     (1, 4, 2, 8, 500, 64, "fp16", False, 3),         # window without causal
