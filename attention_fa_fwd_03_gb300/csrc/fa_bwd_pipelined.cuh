@@ -78,13 +78,15 @@ __device__ __forceinline__ void exp2_scores32(uint32_t (&sv)[32], uint64_t c2, c
 
 // ---------------------------------------------------------------- dK / dV
 // One dK/dV work item: a (batch, KV group) and a block of 128 KV rows; its
-// tiles are the query tiles (of every head of the group) that see the block.
+// tiles are the query tiles (of every head of the group) that see the block,
+// numbered head by head. With the item split over the `split` CTAs of a
+// cluster, CTA `part` takes the tiles [it0, it0 + n_iter) of that list.
 struct DkvItem {
-  int bg, b, g, k0, i_lo, n_qt, n_iter;
+  int bg, b, g, k0, i_lo, n_qt, it0, n_iter;
 };
 
 __device__ __forceinline__ DkvItem dkv_item(int linear, const TileOrder& o, const AttnShape& s,
-                                            int bmq) {
+                                            int bmq, int split = 1, int part = 0) {
   DkvItem t;
   int kvt;
   decode_tile(linear, o, &t.bg, &kvt);
@@ -95,14 +97,23 @@ __device__ __forceinline__ DkvItem dkv_item(int linear, const TileOrder& o, cons
   query_range(s, t.k0, min(s.Tkv, t.k0 + kBM), &qf, &ql);
   t.i_lo = qf / bmq;
   t.n_qt = max(0, (ql + bmq - 1) / bmq - t.i_lo);
-  t.n_iter = t.n_qt * (s.Hq / s.Hkv);
+  const int total = t.n_qt * (s.Hq / s.Hkv);
+  const int share = (total + split - 1) / split;
+  t.it0 = min(total, part * share);
+  t.n_iter = min(total, t.it0 + share) - t.it0;
   return t;
 }
 
-template <int D_, bool BF16_, int NWG_>
+// SPLIT = 2: each work item's tiles are split between the two CTAs of a
+// cluster (for grids with fewer items than half the SMs); CTA 1 leaves its
+// fp32 dK / dV partial sums in its shared memory and CTA 0 adds them to its
+// own through distributed shared memory before it stores. One item per
+// cluster (no cluster launch control).
+template <int D_, bool BF16_, int NWG_, int SPLIT_ = 1>
 struct DkvCfg {
   static constexpr int D = D_;
   static constexpr bool BF16 = BF16_;
+  static constexpr int SPLIT = SPLIT_;
   static constexpr int NWG = NWG_;          // softmax warpgroups
   static constexpr int CW = 128 / NWG;      // score columns per warpgroup
   static constexpr int QST = 3;             // Q ring: needed first by the next tile
@@ -146,6 +157,11 @@ struct DkvCfg {
   static constexpr uint32_t dst_col(int kk) { return chunk_operand_col(DP_COL, kk); }
   static_assert(NWG == 4, "one 32-column chunk per softmax warpgroup");
   static_assert(D <= 128, "dV and dK accumulators share 256 TMEM columns");
+  // CTA 1's partial sums: 128 rows x [dV | dK] fp32 over the tile buffers
+  // (free once the item's MMAs have completed), 16-byte chunks swizzled by row
+  static constexpr int PART_ROW = 2 * D * 4;
+  static_assert(SPLIT == 1 || (SPLIT == 2 && 128 * PART_ROW <= OFF_STATS &&
+                               (PART_ROW / 16) % 8 == 0), "partial sums buffer");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -174,6 +190,15 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   const uint64_t tmo = wc.timeout_cycles;
   const int reps = s.Hq / s.Hkv;
   const ItemQueue iq{sbase + C::OFF_CLC, bar(C::B_CLCFULL), bar(C::B_CLCEMPTY)};
+  // split items: cluster rank and the item of the cluster; otherwise the
+  // CTA's first item, later ones through cluster launch control
+  const int part = C::SPLIT > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int first_item = C::SPLIT > 1 ? static_cast<int>(blockIdx.x) / C::SPLIT : static_cast<int>(blockIdx.x);
+  auto next_item = [&](int k, int* item) {
+    if constexpr (C::SPLIT > 1) return false;
+    return clc_next(iq, k, lane, item, tmo, abort_flag, wc.status);
+  };
+  auto item_of = [&](int item) { return dkv_item(item, order, s, C::BMQ, C::SPLIT, part); };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -224,13 +249,13 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const uint64_t pol_ring = l2_policy_evict_last(), pol_once = l2_policy_evict_first();
     int gt = 0, ln = 0, asked = 0;  // ring tiles issued, items with work, item requests
     bool ok = true;
-    for (int k = 0, item = blockIdx.x; ok; ++k) {
-      if (q_ring) {
+    for (int k = 0, item = first_item; ok; ++k) {
+      if (q_ring && C::SPLIT == 1) {
         ok = clc_request(iq, k, leader, tmo, abort_flag, wc.status);
         if (!ok) break;
         ++asked;
       }
-      const DkvItem t = dkv_item(item, order, s, C::BMQ);
+      const DkvItem t = item_of(item);
       if (t.n_iter > 0) {
         // K (or V) of this KV block, once its previous contents were last read
         if (ln > 0) ok = mbar_wait(bar(once_empty), (ln - 1) & 1, tmo, abort_flag, wc.status);
@@ -240,8 +265,8 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           if (leader) tma_load_3d_hint(once + r * C::REGION, once_map, bar(once_full), r * 64, t.k0, t.bg, pol_once);
         ++ln;
         for (int it = 0; it < t.n_iter; ++it, ++gt) {
-          const int zq = t.b * s.Hq + t.g * reps + it / t.n_qt;
-          const int i0 = (t.i_lo + it % t.n_qt) * C::BMQ;
+          const int zq = t.b * s.Hq + t.g * reps + (t.it0 + it) / t.n_qt;
+          const int i0 = (t.i_lo + (t.it0 + it) % t.n_qt) * C::BMQ;
           const int st = gt % nst;
           if (gt >= nst) ok = mbar_wait(bar(empty + st), ((gt / nst) - 1) & 1, tmo, abort_flag, wc.status);
           if (!ok) break;
@@ -251,7 +276,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
         if (!ok) break;
       }
-      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
+      if (!next_item(k, &item)) break;
     }
     if (*abort_flag) {
       drain_ring(bar(once_full), 1, ln, wc.drain_cycles, wc.status);
@@ -281,8 +306,8 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     };
     int gt = 0, ln = 0;  // tiles before this item, items with work
     bool ok = true;
-    for (int k = 0, item = blockIdx.x; ok; ++k) {
-      const DkvItem t = dkv_item(item, order, s, C::BMQ);
+    for (int k = 0, item = first_item; ok; ++k) {
+      const DkvItem t = item_of(item);
       const int n = t.n_iter;
       if (n > 0) {
         // S^T of the item's first tile: its K block and Q(gt) (the score
@@ -353,7 +378,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         gt += n;
         ++ln;
       }
-      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
+      if (!next_item(k, &item)) break;
     }
     // every issued MMA completes before the CTA exits
     if (leader) mma_commit(bar(C::B_DRAIN));
@@ -363,13 +388,13 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     // a flat stream over the tiles of the CTA's items; each lane loads its
     // four rows of the next tile into registers before waiting for that
     // tile's slot, so the global-load latency hides behind the wait
-    int k = 0, item = blockIdx.x, it = 0;
-    DkvItem t = dkv_item(item, order, s, C::BMQ);
+    int k = 0, item = first_item, it = 0;
+    DkvItem t = item_of(item);
     auto advance = [&]() {  // to the next tile with work; false at the end
       while (it >= t.n_iter) {
-        if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) return false;
+        if (!next_item(k, &item)) return false;
         ++k;
-        t = dkv_item(item, order, s, C::BMQ);
+        t = item_of(item);
         it = 0;
       }
       return true;
@@ -377,8 +402,8 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     constexpr int RPL = C::BMQ / 32;  // rows per lane
     float L[RPL], Dv[RPL];
     auto load = [&]() {
-      const int h = t.g * reps + it / t.n_qt;
-      const int i0 = (t.i_lo + it % t.n_qt) * C::BMQ;
+      const int h = t.g * reps + (t.it0 + it) / t.n_qt;
+      const int i0 = (t.i_lo + (t.it0 + it) % t.n_qt) * C::BMQ;
       const int64_t base = static_cast<int64_t>(t.b * s.Hq + h) * s.Tq;
 #pragma unroll
       for (int r = 0; r < RPL; ++r) {
@@ -422,11 +447,12 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
     int gt = 0, ln = 0;
     bool ok = true;
-    for (int k = 0, item = blockIdx.x; ok; ++k) {
-      const DkvItem t = dkv_item(item, order, s, C::BMQ);
+    for (int k = 0, item = first_item; ok; ++k) {
+      const DkvItem t = item_of(item);
       const int krow = t.k0 + quarter * 32 + lane;  // KV row of this thread (TMEM lane)
       const int i_first = t.i_lo * C::BMQ, i_end = (t.i_lo + t.n_qt) * C::BMQ;
-      int i0 = i_first;  // query tile of this step: the heads of the group in turn
+      // query tile of this step: the heads of the group in turn
+      int i0 = t.n_qt > 0 ? (t.i_lo + t.it0 % t.n_qt) * C::BMQ : i_first;
       for (int it = 0; it < t.n_iter; ++it, i0 = (i0 + C::BMQ == i_end) ? i_first : i0 + C::BMQ) {
         const int gi = gt + it;
         const int slot = gi & 1;
@@ -507,6 +533,35 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (!ok) break;
         tc_fence_after();
       }
+      if constexpr (C::SPLIT > 1) {
+        // CTA 1: its partial sums to its own shared memory (the tile buffers
+        // are free: the item's MMAs have completed); CTA 0 adds them after the
+        // cluster barrier at the end
+        if (part == 1) {
+          const int row = quarter * 32 + lane;
+#pragma unroll 1
+          for (int c = wg; c < C::PART_ROW / 64; c += C::NWG) {  // 16-column chunks
+            uint32_t v[16];
+            if (have) {
+              tmem_ld16(tmem + lane_base + C::DV_COL + 16 * c, v);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] = 0u;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(smem + row * C::PART_ROW + (((4 * c + q) ^ (row & 7)) << 4)) =
+                  make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          }
+        }
+        if (have) {
+          tc_fence_before();
+          gt += t.n_iter;
+          ++ln;
+        }
+        break;  // one item per cluster
+      }
       // blocks of W columns of [dV | dK] dealt round-robin over the warps of
       // this lane quarter
       constexpr int S = (C::D % 64 == 0 && 2 * C::D / 64 >= C::NWG) ? 8 : 4, W = 8 * S;
@@ -526,8 +581,61 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         gt += t.n_iter;
         ++ln;
       }
-      if (!clc_next(iq, k, lane, &item, tmo, abort_flag, wc.status)) break;
+      if (!next_item(k, &item)) break;
     }
+  }
+
+  if constexpr (C::SPLIT > 1) {
+    // every thread of both CTAs: CTA 1's partial sums are in its shared memory
+    cluster_barrier();
+    if (part == 0 && warp >= 4 && !*abort_flag) {
+      // CTA 0: its accumulators plus CTA 1's partial sums, rounded and stored
+      // (dK scaled); 16-column chunks dealt over the softmax warpgroups
+      const DkvItem t = item_of(first_item);
+      const int wg = (warp - 4) >> 2, quarter = warp & 3;
+      const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+      const int row = quarter * 32 + lane, krow = t.k0 + row;
+      const bool have = t.n_iter > 0;
+      using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
+#pragma unroll 1
+      for (int c = wg; c < C::PART_ROW / 64; c += C::NWG) {
+        uint32_t v[16];
+        if (have) {
+          tc_fence_after();
+          tmem_ld16(tmem + lane_base + C::DV_COL + 16 * c, v);
+          tmem_ld_wait();
+        }
+        float x[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          const uint32_t remote = peer_addr(sbase + row * C::PART_ROW + (((4 * c + q) ^ (row & 7)) << 4), 1);
+          asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(remote));
+          x[4 * q] = __uint_as_float(w.x);
+          x[4 * q + 1] = __uint_as_float(w.y);
+          x[4 * q + 2] = __uint_as_float(w.z);
+          x[4 * q + 3] = __uint_as_float(w.w);
+        }
+        const bool is_dk = 16 * c >= C::D;
+        const float mul = is_dk ? scale : 1.f;
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          const float a = (have ? __uint_as_float(v[e]) : 0.f) + x[e];
+          const float b2 = (have ? __uint_as_float(v[e + 1]) : 0.f) + x[e + 1];
+          o[e / 2] = pack2<C::BF16>(a * mul, b2 * mul);
+        }
+        if (krow < s.Tkv) {
+          T16* dst = reinterpret_cast<T16*>(is_dk ? dk_out : dv_out) +
+                     (static_cast<int64_t>(t.bg) * s.Tkv + krow) * C::D + (is_dk ? 16 * c - C::D : 16 * c);
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+      }
+    }
+    // CTA 1 keeps its shared memory until CTA 0 has read it
+    cluster_barrier();
   }
 
   tc_fence_before();

@@ -129,6 +129,43 @@ cudaError_t launch_dkv_with(const BwdLaunch& a, Kern kern) {
   return cudaGetLastError();
 }
 
+// dK/dV with each item's tiles split over the two CTAs of a cluster (one item
+// per cluster, heaviest first): for grids with at most half as many items as
+// SMs.
+template <class C>
+cudaError_t launch_dkv_split(const BwdLaunch& a) {
+  const int bhq = a.s.B * a.s.Hq, bhkv = a.s.B * a.s.Hkv;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_tile_map(&mq, a.q, C::BF16, C::D, a.s.Tq, bhq, C::BMQ) ||
+      !encode_tile_map(&mdo, a.dout, C::BF16, C::D, a.s.Tq, bhq, C::BMQ) ||
+      !encode_tile_map(&mk, a.k, C::BF16, C::D, a.s.Tkv, bhkv, kBM) ||
+      !encode_tile_map(&mv, a.v, C::BF16, C::D, a.s.Tkv, bhkv, kBM))
+    return cudaErrorInvalidValue;
+  auto kern = fa_bwd_dkv_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const TileOrder order = kv_block_order(a.s, C::D);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(C::SPLIT * order.units * order.tiles), 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C::SPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, a.lse, static_cast<const float*>(a.dvec),
+                            a.dk, a.dv, a.scale, a.s, order, a.wc);
+}
+
+inline bool dkv_small_grid(const AttnShape& s) {
+  return 2 * static_cast<int64_t>(s.B) * s.Hkv * ((s.Tkv + kBM - 1) / kBM) <= device_sm_count();
+}
+
 // D = 256 dK/dV: one cluster of two CTAs per 128-row KV block
 // (fa_bwd_dkv_pair_kernel), non-persistent, heaviest blocks first.
 template <class C>
@@ -192,7 +229,10 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
   if (phases & kPhaseDkv) {
     if constexpr (D <= 128) {
       using C = DkvCfg<D, BF16, kSoftmaxWarpgroups>;
-      e = launch_dkv_with<C>(a, fa_bwd_dkv_kernel<C>);
+      if (dkv_small_grid(a.s))
+        e = launch_dkv_split<DkvCfg<D, BF16, kSoftmaxWarpgroups, 2>>(a);
+      else
+        e = launch_dkv_with<C>(a, fa_bwd_dkv_kernel<C>);
     } else {
       e = launch_dkv_pair<DkvPairCfg<BF16>>(a);
     }
