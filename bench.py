@@ -292,6 +292,42 @@ def oracle_sample(w, target_s: float):
 
 
 # ---------------------------------------------------------------- our path
+def host_link(hosts, outs, dev_bufs, s_in, s_out, reps: int = 3) -> dict:
+    """Host <-> device copy rates of one step's tensors over pinned buffers:
+    inputs in alone, outputs out alone, and both directions at once (ms per
+    step's worth of bytes; GB/s)."""
+    import torch
+
+    def timed(copy_in: bool, copy_out: bool) -> float:
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_in)
+            s_out.wait_event(e0)
+            if copy_in:
+                with torch.cuda.stream(s_in):
+                    for n, t in hosts.items():
+                        dev_bufs[n].copy_(t, non_blocking=True)
+            if copy_out:
+                with torch.cuda.stream(s_out):
+                    for n, t in outs.items():
+                        t.copy_(dev_bufs[n], non_blocking=True)
+            s_in.wait_stream(s_out)
+            e1.record(s_in)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    bi = sum(t.numel() * t.element_size() for t in hosts.values())
+    bo = sum(t.numel() * t.element_size() for t in outs.values())
+    t_in, t_out, t_both = timed(True, False), timed(False, True), timed(True, True)
+    return {"h2d_ms": round(t_in, 4), "h2d_gbs": round(bi / t_in / 1e6, 1),
+            "d2h_ms": round(t_out, 4), "d2h_gbs": round(bo / t_out / 1e6, 1),
+            "both_ms": round(t_both, 4), "both_gbs": round((bi + bo) / t_both / 1e6, 1)}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import attention_fa_fwd_03_gb300 as fa
@@ -417,12 +453,17 @@ def run_ours(args, rank, world, local_rank):
         e1.record(s_out)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+        link = host_link(hosts, outs, bufs[0], s_in, s_out)
         e2e = {"value": round(job_tflops(world, 1, fwd_f + bwd_f, e2e_ms), 2),
                "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "api": "fa_fwd + fa_bwd (C ABI via the Python binding), pinned host buffers; "
                       "copy-in, compute and copy-out on three streams over two buffer sets, "
-                      "so step i's inputs load while step i-1 computes"}
+                      "so step i's inputs load while step i-1 computes",
+               "link": link,
+               "bound_ms": round(max(link["both_ms"], sum(step_ms) / len(step_ms)), 4),
+               "bound_note": "an end-to-end step takes at least the longer of the step's "
+                             "copies in both directions at once and its compute"}
 
     if rank != 0:
         return None

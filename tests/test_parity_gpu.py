@@ -248,6 +248,13 @@ EDGE = [
     # grids large enough for two 128-row query tiles per forward CTA, ragged tails
     (4, 40, 8, 300, 300, 128, "bf16", True, 0),
     (2, 80, 10, 200, 260, 64, "fp16", False, 70),
+    # small grids: each KV block's tiles split over a two-CTA cluster
+    (1, 4, 1, 700, 700, 64, "fp16", True, 200),      # causal window, 4 heads per group
+    (2, 6, 2, 333, 500, 128, "bf16", False, 0),      # 3 heads per group, Tq != Tkv
+    (1, 2, 2, 500, 500, 96, "fp16", True, 0),        # one head per group: split by query tiles
+    # head dim 256: two-CTA dK/dV clusters, dQ with Q in TMEM
+    (1, 2, 1, 300, 100, 256, "bf16", True, 40),      # fully masked rows
+    (1, 8, 2, 260, 300, 256, "fp16", False, 50),     # window without causal, 4 heads per group
     # short query blocks (Tq <= 8): the split-key forward
     (1, 4, 2, 6, 300, 128, "bf16", True, 0),         # causal, top-left: row i sees i + 1 keys
     (1, 4, 2, 8, 500, 64, "fp16", False, 3),         # window without causal
