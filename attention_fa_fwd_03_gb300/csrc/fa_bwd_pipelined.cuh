@@ -1092,7 +1092,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
               fadd2(f2_pack(__uint_as_float(pv[q]), __uint_as_float(pv[q + 1])), ndx2);
           const float2 d2 = f2_unpack(
               fmul2(d, f2_pack(__uint_as_float(sv[q]), __uint_as_float(sv[q + 1]))));
-          dsv[q / 2] = pack2<C::BF16>(d2.x, d2.y);
+          dsv[q / 2] = pack2_rna<C::BF16>(d2.x, d2.y);
         }
         tmem_st16(tmem + lane_base + col, dsv);
         tmem_st_wait();

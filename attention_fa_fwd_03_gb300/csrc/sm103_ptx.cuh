@@ -517,6 +517,23 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// As pack2, with the bf16 rounding done on the integer pipe: round to nearest
+// with ties away from zero by one integer add on each fp32 bit pattern, then a
+// byte permute that keeps the two high halves (three integer instructions per
+// pair instead of one cvt.rn.bf16x2.f32, which runs at 16 instructions per
+// clock per SM on GB300, half the rate of ex2.approx). It differs from cvt.rn
+// only on exact ties (low 16 bits 0x8000). fp16 keeps the conversion. Used
+// for dS in the dQ kernel (4% faster there); in the forward and dK/dV softmax
+// loops the extra integer instructions cost more than they save (measured).
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack2_rna(float lo, float hi) {
+  if constexpr (kBF16) {
+    return __byte_perm(__float_as_uint(lo) + 0x8000u, __float_as_uint(hi) + 0x8000u, 0x7632);
+  } else {
+    return pack2<false>(lo, hi);
+  }
+}
+
 template <bool kBF16>
 __device__ __forceinline__ float2 unpack2(uint32_t w) {
   if constexpr (kBF16) {
