@@ -619,3 +619,232 @@ fa_bwd_dq_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
 }
 
 }  // namespace fa
+
+namespace fa {
+
+// ---------------------------------------------------------------------------
+// dK / dV for short query blocks: the vector VJP that page "[Metal] Add Flash
+// Attention VJP for training" names for short sequences (Key Features: fp32
+// dK/dV accumulation per key row, no padded tiles), computing backward pass 2
+// of page "mlx-bun 0.0.4: package/src/model/flash-attention.ts":
+//   dV_j = sum_i P_ij dO_i,   dK_j = scale * sum_i dS_ij Q_i,
+//   P_ij = exp(S_ij - L_i),   dS_ij = P_ij (dO_i . V_j - D_i),
+// the sums running over the query rows of every head that shares key j (GQA).
+//
+// GB300 design (not the pages'): with Tq <= 8 a KV group has at most 8 r query
+// rows, so a 128-row tensor-core tile is mostly padding, and with a causal or
+// window mask the heads' rows cannot be folded into one tile either (the mask
+// depends on each row's position within its head). One CTA takes kVecKeys
+// keys of one (batch, KV group) and walks the group's query rows in chunks of
+// RC (8, 16 or 32), staged in shared memory as fp32 (Q pre-scaled by
+// scale log2 e):
+//   1. S and dP: a lane per key, RC / 8 rows per warp, dot
+//      products over D read 16 bytes at a time (K / V rows padded to D + 4
+//      floats, so the lanes' rows fall on distinct banks; the row vectors are
+//      broadcast);
+//   2. P = 2^(S - L log2 e), zero where the mask hides the key from the row's
+//      position (or the row has no visible key), and dS = P (dP - D);
+//   3. dV_j += P_ij dO_i and dK_j += dS_ij Q_i in fp32 registers, 8 threads
+//      per key, each 4 consecutive columns per 32.
+// dK is divided by log2 e at the end and both are written in the input dtype.
+// Keys that no query position sees are written as zeros.
+constexpr int kVecKeys = 32;     // keys per CTA
+constexpr int kVecThreads = 256;
+
+// RC: query rows per chunk (8, 16 or 32: the group's rows rounded up, at most 32)
+template <int D_, bool BF16_, int RC_>
+struct DkvVecCfg {
+  static constexpr int D = D_;
+  static constexpr bool BF16 = BF16_;
+  static constexpr int RC = RC_;
+  static constexpr int KS = D + 4;                  // fp32 stride of a K / V row
+  static constexpr int PS = RC + 1;           // stride of a P / dS row (one per key)
+  static constexpr int F_K = 0;                     // [kVecKeys][KS]
+  static constexpr int F_V = F_K + kVecKeys * KS;   // [kVecKeys][KS]
+  static constexpr int F_Q = F_V + kVecKeys * KS;   // [RC][D] Q * scale * log2 e
+  static constexpr int F_DO = F_Q + RC * D;   // [RC][D]
+  static constexpr int F_NL = F_DO + RC * D;  // [RC] -L log2 e (-inf: P = 0)
+  static constexpr int F_DV = F_NL + RC;      // [RC] D-vector
+  static constexpr int F_POS = F_DV + RC;     // [RC] position within the head (int)
+  static constexpr int F_P = F_POS + RC;      // [kVecKeys][PS]
+  static constexpr int F_DS = F_P + kVecKeys * PS;  // [kVecKeys][PS]
+  static constexpr int F_END = F_DS + kVecKeys * PS;
+  static constexpr int SMEM_BYTES = F_END * 4;
+  static constexpr int NG = D / 32;                 // 4-column groups a thread accumulates
+  static_assert(D % 32 == 0, "head dim");
+  static_assert(kVecThreads == 8 * kVecKeys && RC % 8 == 0 && RC <= 32, "thread roles");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+template <class C>
+__global__ void __launch_bounds__(kVecThreads)
+fa_bwd_dkv_vec_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                      const uint16_t* __restrict__ v, const uint16_t* __restrict__ dout,
+                      const float* __restrict__ lse, const float* __restrict__ dvec,
+                      uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, AttnShape s) {
+  extern __shared__ __align__(16) float sm[];
+  constexpr int D = C::D;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int nblk = (s.Tkv + kVecKeys - 1) / kVecKeys;
+  const int zkv = blockIdx.x / nblk;  // b * Hkv + g
+  const int j0 = (blockIdx.x - zkv * nblk) * kVecKeys;
+  const int b = zkv / s.Hkv, g = zkv - b * s.Hkv;
+  const int reps = s.Hq / s.Hkv;
+  const int rows = reps * s.Tq;       // query rows of the group
+  int* smi = reinterpret_cast<int*>(sm);
+  // accumulation role: key jj, columns c4 .. c4 + 3 of every 32
+  const int jj = t >> 3, c4 = (t & 7) * 4;
+  float adk[C::NG][4], adv[C::NG][4];
+#pragma unroll
+  for (int m = 0; m < C::NG; ++m)
+#pragma unroll
+    for (int x = 0; x < 4; ++x) adk[m][x] = adv[m][x] = 0.f;
+  int kf, kl;
+  key_range(s, 0, s.Tq, &kf, &kl);
+  if (j0 < kl && j0 + kVecKeys > kf) {
+    // Global loads are issued together (16 bytes each, into registers) and
+    // converted afterwards, so staging costs one memory round trip, not one
+    // per loop trip.
+    constexpr int VPR = D / 8;  // 16-byte vectors per row
+    constexpr int NKV = (kVecKeys * VPR + kVecThreads - 1) / kVecThreads;
+    constexpr int NQR = (C::RC * VPR + kVecThreads - 1) / kVecThreads;
+    auto row_of = [&](int gi) {  // global row of the group's query row gi
+      const int hh = gi / s.Tq;
+      return (static_cast<int64_t>(b) * s.Hq + g * reps + hh) * s.Tq + (gi - hh * s.Tq);
+    };
+    auto put8 = [&](float* dst, uint4 w, float mul) {  // dst 16-byte aligned
+      const float2 a0 = unpack2<C::BF16>(w.x), a1 = unpack2<C::BF16>(w.y);
+      const float2 a2 = unpack2<C::BF16>(w.z), a3 = unpack2<C::BF16>(w.w);
+      reinterpret_cast<float4*>(dst)[0] = make_float4(a0.x * mul, a0.y * mul, a1.x * mul, a1.y * mul);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(a2.x * mul, a2.y * mul, a3.x * mul, a3.y * mul);
+    };
+    // K and V rows of the block (rows past Tkv are zero)
+    {
+      uint4 kw[NKV], vw[NKV];
+#pragma unroll
+      for (int n = 0; n < NKV; ++n) {
+        const int e = t + n * kVecThreads, j = e / VPR;
+        kw[n] = vw[n] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < kVecKeys * VPR && j0 + j < s.Tkv) {
+          const int64_t at = (static_cast<int64_t>(zkv) * s.Tkv + j0 + j) * D + (e - j * VPR) * 8;
+          kw[n] = *reinterpret_cast<const uint4*>(k + at);
+          vw[n] = *reinterpret_cast<const uint4*>(v + at);
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < NKV; ++n) {
+        const int e = t + n * kVecThreads, j = e / VPR;
+        if (e < kVecKeys * VPR) {
+          put8(sm + C::F_K + j * C::KS + (e - j * VPR) * 8, kw[n], 1.f);
+          put8(sm + C::F_V + j * C::KS + (e - j * VPR) * 8, vw[n], 1.f);
+        }
+      }
+    }
+    for (int i0 = 0; i0 < rows; i0 += C::RC) {
+      uint4 qw[NQR], ow[NQR];
+#pragma unroll
+      for (int n = 0; n < NQR; ++n) {
+        const int e = t + n * kVecThreads, i = e / VPR;
+        qw[n] = ow[n] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < C::RC * VPR && i0 + i < rows) {
+          const int64_t at = row_of(i0 + i) * D + (e - i * VPR) * 8;
+          qw[n] = *reinterpret_cast<const uint4*>(q + at);
+          ow[n] = *reinterpret_cast<const uint4*>(dout + at);
+        }
+      }
+      float nl = -INFINITY, dd = 0.f;
+      int pos = 0;
+      if (t < C::RC && i0 + t < rows) {
+        const int gi = i0 + t;
+        pos = gi % s.Tq;
+        const int64_t row = row_of(gi);
+        const float L = lse[row];
+        if (L != -INFINITY) nl = -L * kLog2e;
+        dd = dvec[row];
+      }
+      __syncthreads();  // the previous chunk's rows, P and dS are consumed
+#pragma unroll
+      for (int n = 0; n < NQR; ++n) {
+        const int e = t + n * kVecThreads, i = e / VPR;
+        if (e < C::RC * VPR) {
+          put8(sm + C::F_Q + i * D + (e - i * VPR) * 8, qw[n], s.scale_log2);
+          put8(sm + C::F_DO + i * D + (e - i * VPR) * 8, ow[n], 1.f);
+        }
+      }
+      if (t < C::RC) {
+        sm[C::F_NL + t] = nl;
+        sm[C::F_DV + t] = dd;
+        smi[C::F_POS + t] = pos;
+      }
+      __syncthreads();
+      {
+        // S (log2 domain) and dP of key `lane` against rows warp + 8 x (x < RC / 8)
+        const float* kr = sm + C::F_K + lane * C::KS;
+        const float* vr = sm + C::F_V + lane * C::KS;
+        constexpr int RW = C::RC / 8;  // rows per warp
+        float sa[RW], pa[RW];
+#pragma unroll
+        for (int x = 0; x < RW; ++x) sa[x] = pa[x] = 0.f;
+#pragma unroll 4
+        for (int d = 0; d < D; d += 4) {
+          const float4 k4 = *reinterpret_cast<const float4*>(kr + d);
+          const float4 v4 = *reinterpret_cast<const float4*>(vr + d);
+#pragma unroll
+          for (int x = 0; x < RW; ++x) {
+            const int i = warp + 8 * x;
+            const float4 q4 = *reinterpret_cast<const float4*>(sm + C::F_Q + i * D + d);
+            const float4 o4 = *reinterpret_cast<const float4*>(sm + C::F_DO + i * D + d);
+            sa[x] = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, fmaf(q4.w, k4.w, sa[x]))));
+            pa[x] = fmaf(o4.x, v4.x, fmaf(o4.y, v4.y, fmaf(o4.z, v4.z, fmaf(o4.w, v4.w, pa[x]))));
+          }
+        }
+        const int key = j0 + lane;
+#pragma unroll
+        for (int x = 0; x < RW; ++x) {
+          const int i = warp + 8 * x;
+          const float nl = sm[C::F_NL + i];
+          const bool vis = key < s.Tkv && nl != -INFINITY &&
+                           key_visible(smi[C::F_POS + i], key, s.causal, s.window);
+          const float p = vis ? ex2(sa[x] + nl) : 0.f;
+          sm[C::F_P + lane * C::PS + i] = p;
+          sm[C::F_DS + lane * C::PS + i] = p * (pa[x] - sm[C::F_DV + i]);
+        }
+      }
+      __syncthreads();
+#pragma unroll 4
+      for (int i = 0; i < C::RC; ++i) {
+        const float p = sm[C::F_P + jj * C::PS + i], ds = sm[C::F_DS + jj * C::PS + i];
+#pragma unroll
+        for (int m = 0; m < C::NG; ++m) {
+          const int d = 32 * m + c4;
+          const float4 o4 = *reinterpret_cast<const float4*>(sm + C::F_DO + i * D + d);
+          const float4 q4 = *reinterpret_cast<const float4*>(sm + C::F_Q + i * D + d);
+          adv[m][0] = fmaf(p, o4.x, adv[m][0]);
+          adv[m][1] = fmaf(p, o4.y, adv[m][1]);
+          adv[m][2] = fmaf(p, o4.z, adv[m][2]);
+          adv[m][3] = fmaf(p, o4.w, adv[m][3]);
+          adk[m][0] = fmaf(ds, q4.x, adk[m][0]);
+          adk[m][1] = fmaf(ds, q4.y, adk[m][1]);
+          adk[m][2] = fmaf(ds, q4.z, adk[m][2]);
+          adk[m][3] = fmaf(ds, q4.w, adk[m][3]);
+        }
+      }
+    }
+  }
+  const int key = j0 + jj;
+  if (key < s.Tkv) {
+    const int64_t base = (static_cast<int64_t>(zkv) * s.Tkv + key) * D;
+#pragma unroll
+    for (int m = 0; m < C::NG; ++m) {
+      const int d = 32 * m + c4;
+      const uint2 wk = make_uint2(pack2<C::BF16>(adk[m][0] * kLn2, adk[m][1] * kLn2),
+                                  pack2<C::BF16>(adk[m][2] * kLn2, adk[m][3] * kLn2));
+      const uint2 wv = make_uint2(pack2<C::BF16>(adv[m][0], adv[m][1]),
+                                  pack2<C::BF16>(adv[m][2], adv[m][3]));
+      *reinterpret_cast<uint2*>(dk + base + d) = wk;
+      *reinterpret_cast<uint2*>(dv + base + d) = wv;
+    }
+  }
+}
+
+}  // namespace fa

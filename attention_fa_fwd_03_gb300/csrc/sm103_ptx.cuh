@@ -84,7 +84,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // A wait bound below this many cycles (a test of the give-up path) also reads
-// the clock after every failed try, so the wait gives up at its first miss.
+// the clock after every failed try and never suspends, so the wait gives up
+// at its first miss.
 constexpr uint64_t kShortWaitCycles = 1024;
 
 // As mbar_wait below, but polling with test_wait: for the single thread that
@@ -118,15 +119,18 @@ __device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity,
 // must not be cut short by an earlier abort).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_cycles,
                                           volatile int* abort, uint32_t* status) {
-  const int tries = timeout_cycles < kShortWaitCycles ? 1 : 32;
+  // a bound below kShortWaitCycles tests without suspending (try_wait may hold
+  // the thread until the phase completes, so such a wait would never miss)
+  const bool short_bound = timeout_cycles < kShortWaitCycles;
+  const int tries = short_bound ? 1 : 32;
 #pragma unroll 1
   for (int i = 0; i < tries; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+    if (short_bound ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < tries; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (short_bound ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
     if (static_cast<uint64_t>(clock64() - t0) > timeout_cycles) {
       if (abort != nullptr) *abort = 1;

@@ -264,6 +264,11 @@ EDGE = [
     (1, 16, 1, 3, 2000, 64, "bf16", False, 0),       # GQA 16:1
     (1, 8, 1, 1, 20000, 128, "bf16", False, 0),      # decode over a long key range
     (1, 4, 2, 8, 9000, 96, "fp16", False, 1000),     # long keys, window 1000 (past only)
+    # short query blocks: the vector dK/dV (rows of all the group's heads, any mask)
+    (2, 16, 2, 8, 100, 256, "bf16", True, 0),        # 64 rows per group (two chunks), D=256
+    (1, 12, 4, 5, 3, 64, "fp16", True, 0),           # fewer keys than query rows, causal
+    (1, 8, 2, 7, 1500, 128, "bf16", True, 3),        # causal window of 3
+    (2, 32, 2, 8, 64, 96, "fp16", False, 5),         # 128 rows per group, window without causal
     # mask-free GQA below one tile: the heads' rows share tiles
     (2, 8, 2, 40, 300, 128, "bf16", False, 0),       # 4 x 40 rows per group
     (1, 6, 2, 100, 200, 64, "fp16", False, 0),       # 3 x 100 rows, ragged tiles
