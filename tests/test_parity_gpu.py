@@ -252,6 +252,10 @@ EDGE = [
     (1, 4, 1, 700, 700, 64, "fp16", True, 200),      # causal window, 4 heads per group
     (2, 6, 2, 333, 500, 128, "bf16", False, 0),      # 3 heads per group, Tq != Tkv
     (1, 2, 2, 500, 500, 96, "fp16", True, 0),        # one head per group: split by query tiles
+    # small causal / windowed grids with a heavy first block: four-CTA clusters
+    (1, 4, 1, 1024, 1024, 64, "fp16", True, 0),      # 8 blocks of 4-32 tiles
+    (1, 8, 2, 700, 700, 128, "bf16", True, 256),     # causal window
+    (2, 6, 2, 900, 900, 96, "fp16", True, 0),        # 3 heads per group, ragged tail
     # head dim 256: two-CTA dK/dV clusters, dQ with Q in TMEM
     (1, 2, 1, 300, 100, 256, "bf16", True, 40),      # fully masked rows
     (1, 8, 2, 260, 300, 256, "fp16", False, 50),     # window without causal, 4 heads per group
