@@ -44,6 +44,12 @@
 //           also sends each tile's P buffer to the peer
 //   warps 4-11  two softmax warpgroups, 32 query columns each; they also
 //           write the item's K or V rows into TMEM and store the accumulator.
+// HALVES = 2 (grids where one causal block's tiles would be the critical
+// path): a cluster of four CTAs, two such pairs (ranks 0-1 and 2-3), each
+// taking half of the block's query tiles; pair 1 leaves its fp32
+// accumulators in its own shared memory (the rings are free once its MMAs
+// have completed) and pair 0 adds them, rank r from rank r + 2, through
+// distributed shared memory before it stores.
 #pragma once
 
 #include <type_traits>
@@ -53,10 +59,13 @@
 
 namespace fa {
 
-template <bool BF16_>
+template <bool BF16_, int HALVES_ = 1>
 struct DkvPairCfg {
   static constexpr int D = 256;
   static constexpr bool BF16 = BF16_;
+  static constexpr int HALVES = HALVES_;        // pairs sharing a block's query tiles
+  static constexpr int CLUSTER = 2 * HALVES;    // CTAs per cluster
+  static constexpr int PART_ROW = D * 4;        // a row of fp32 partial sums (pair 1)
   static constexpr int BMQ = 64;              // query rows per tile (N of the score MMAs)
   static constexpr int NWG = 2;               // softmax warpgroups, 32 query columns each
   static constexpr int RST = 3;               // depth of both rings
@@ -92,10 +101,12 @@ struct DkvPairCfg {
   static_assert(SC_COL0 + 2 * BMQ <= ACC_COL && ACC_COL + D <= 512, "TMEM budget");
   static_assert(BMQ == 32 * NWG, "one 32-column chunk per softmax warpgroup");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(HALVES == 1 || (HALVES == 2 && 128 * PART_ROW <= OFF_PBUF), "partial sums");
 };
 
+// Launched with a cluster of C::CLUSTER CTAs (cudaLaunchKernelEx).
 template <class C>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::THREADS, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
 fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                        const void* __restrict__ k_rows, const void* __restrict__ v_rows,
                        const float* __restrict__ lse, const float* __restrict__ dvec,
@@ -103,8 +114,10 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
                        AttnShape s, TileOrder order, WaitCfg wc) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t rank = cluster_ctarank();  // 0: P side, 1: dS side
-  const bool pside = rank == 0;
+  const uint32_t rank = cluster_ctarank();   // even: P side, odd: dS side
+  const bool pside = (rank & 1u) == 0;
+  const uint32_t peer = rank ^ 1u;            // the other side of this pair
+  const int pair = static_cast<int>(rank >> 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -114,7 +127,8 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
   float* stats = reinterpret_cast<float*>(smem + C::OFF_STATS);
   const uint64_t tmo = wc.timeout_cycles;
   const int reps = s.Hq / s.Hkv;
-  const DkvItem t = dkv_item(static_cast<int>(blockIdx.x >> 1), order, s, C::BMQ);
+  const DkvItem t = dkv_item(static_cast<int>(blockIdx.x) / C::CLUSTER, order, s, C::BMQ,
+                             C::HALVES, pair);
   const int n = t.n_iter;
   const bool aligned = (sbase & 1023u) == 0;  // the 128-byte swizzle needs it
 
@@ -141,8 +155,8 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
   }
   tc_fence_before();
   __syncthreads();
-  // both CTAs have initialised their barriers before either arrives on the
-  // peer's or writes into its shared memory
+  // every CTA has initialised its barriers before any arrives on a peer's or
+  // writes into its shared memory
   cluster_barrier();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -162,8 +176,8 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
     int it = 0;
     bool ok = !*abort_flag;
     for (; ok && it < n; ++it) {
-      const int zq = t.b * s.Hq + t.g * reps + it / t.n_qt;
-      const int i0 = (t.i_lo + it % t.n_qt) * C::BMQ;
+      const int zq = t.b * s.Hq + t.g * reps + (t.it0 + it) / t.n_qt;
+      const int i0 = (t.i_lo + (t.it0 + it) % t.n_qt) * C::BMQ;
       const int st = it % C::RST;
       if (it >= C::RST) ok = mbar_wait(bar(empty + st), ((it / C::RST) - 1) & 1, tmo, abort_flag, wc.status);
       if (!ok) break;
@@ -235,8 +249,8 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
     constexpr int RPL = C::BMQ / 32;
     float v[RPL];
     auto load = [&](int it) {
-      const int h = t.g * reps + it / t.n_qt;
-      const int i0 = (t.i_lo + it % t.n_qt) * C::BMQ;
+      const int h = t.g * reps + (t.it0 + it) / t.n_qt;
+      const int i0 = (t.i_lo + (t.it0 + it) % t.n_qt) * C::BMQ;
       const int64_t base = static_cast<int64_t>(t.b * s.Hq + h) * s.Tq;
 #pragma unroll
       for (int r = 0; r < RPL; ++r) {
@@ -257,7 +271,7 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
       const int b = j & 1;
       if (!mbar_wait(bar(C::B_STAGED + b), (j >> 1) & 1, tmo, abort_flag, wc.status)) return false;
       const uint32_t buf = sbase + C::OFF_PBUF + b * C::PBUF;
-      if (leader) bulk_copy_to_peer(peer_addr(buf, 1), buf, C::PBUF, peer_addr(bar(C::B_PBUF + b), 1));
+      if (leader) bulk_copy_to_peer(peer_addr(buf, peer), buf, C::PBUF, peer_addr(bar(C::B_PBUF + b), peer));
       __syncwarp();
       return true;
     };
@@ -281,7 +295,7 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
     // the peer drains exactly the copies that were issued if it gives up; the
     // count reaches it through the cluster barrier at exit
     if (pside && leader) {
-      const uint32_t remote = peer_addr(smem_u32(const_cast<int*>(peer_sent)), 1);
+      const uint32_t remote = peer_addr(smem_u32(const_cast<int*>(peer_sent)), peer);
       asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(sent) : "memory");
     }
   } else {
@@ -329,7 +343,7 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
       mbar_arrive_expect_tx(bar(C::B_PBUF + 1), C::PBUF);
     }
     const int i_first = t.i_lo * C::BMQ, i_end = (t.i_lo + t.n_qt) * C::BMQ;
-    int i0 = i_first;
+    int i0 = (t.i_lo + t.it0 % max(t.n_qt, 1)) * C::BMQ;  // the pair's first tile
     for (int j = 0; ok && j < n; ++j, i0 = (i0 + C::BMQ == i_end) ? i_first : i0 + C::BMQ) {
       const int b = j & 1, slot = j & 1;
       ok = mbar_wait(bar(C::B_STFULL + slot), (j >> 1) & 1, tmo, abort_flag, wc.status) &&
@@ -417,7 +431,7 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         if (lane == 0) {
           mbar_arrive(bar(C::B_READY + b));
           mbar_arrive(bar(C::B_STEMPTY + slot));
-          mbar_arrive_peer_relaxed(peer_addr(bar(C::B_PBUF + b), 0));  // the peer's "P buffer b free"
+          mbar_arrive_peer_relaxed(peer_addr(bar(C::B_PBUF + b), peer));  // the peer's "P buffer b free"
         }
       }
     }
@@ -429,7 +443,26 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
       ok = mbar_wait(bar(C::B_DONE), 0, tmo, abort_flag, wc.status);
       if (ok) tc_fence_after();
     }
-    if (ok) {
+    if (ok && C::HALVES == 2 && pair == 1) {
+      // pair 1: its fp32 accumulator rows into its own shared memory (16-byte
+      // chunks swizzled by the row), read by pair 0 after the cluster barrier
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        const int col = 128 * wg + 16 * c;
+        uint32_t v[16];
+        if (have) {
+          tmem_ld16(tmem + lane_base + C::ACC_COL + col, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = 0u;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(smem + r * C::PART_ROW + (((col / 4 + q) ^ (r & 7)) << 4)) =
+              make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+    } else if (ok && C::HALVES == 1) {
       const int row0 = t.k0 + quarter * 32;
       const int rows_valid = min(32, s.Tkv - row0);
       const int64_t orow = static_cast<int64_t>(t.bg) * s.Tkv + (rows_valid > 0 ? row0 : 0);
@@ -452,6 +485,55 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
   if (!pside && warp == 4 && lane == 0 && *abort_flag)
     for (int j = seen; j < *peer_sent; ++j)
       mbar_wait_cluster(bar(C::B_PBUF + (j & 1)), (j >> 1) & 1, wc.drain_cycles, nullptr, wc.status);
+  if constexpr (C::HALVES == 2) {
+    // pair 0: its accumulator plus pair 1's partial sums (rank r reads rank
+    // r + 2, written before the cluster barrier above), scaled, rounded and
+    // stored; 16-column chunks, each warpgroup half of the columns
+    if (pair == 0 && warp >= 4 && !*abort_flag) {
+      const int wg = (warp - 4) >> 2, quarter = warp & 3;
+      const int r = quarter * 32 + lane, krow = t.k0 + r;
+      const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+      const bool have = n > 0;
+      const float mul = pside ? 1.f : scale;
+      using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
+      T16* out = reinterpret_cast<T16*>(pside ? dv_out : dk_out) +
+                 (static_cast<int64_t>(t.bg) * s.Tkv + krow) * C::D;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        const int col = 128 * wg + 16 * c;
+        uint32_t v[16];
+        if (have) {
+          tmem_ld16(tmem + lane_base + C::ACC_COL + col, v);
+          tmem_ld_wait();
+        }
+        float x[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = have ? __uint_as_float(v[e]) : 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          const uint32_t remote =
+              peer_addr(sbase + r * C::PART_ROW + (((col / 4 + q) ^ (r & 7)) << 4), rank + 2u);
+          asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(remote));
+          x[4 * q] += __uint_as_float(w.x);
+          x[4 * q + 1] += __uint_as_float(w.y);
+          x[4 * q + 2] += __uint_as_float(w.z);
+          x[4 * q + 3] += __uint_as_float(w.w);
+        }
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) o[e / 2] = pack2<C::BF16>(x[e] * mul, x[e + 1] * mul);
+        if (krow < s.Tkv) {
+          reinterpret_cast<uint4*>(out + col)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          reinterpret_cast<uint4*>(out + col)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+      }
+    }
+    // pair 1 keeps its shared memory until pair 0 has read it
+    cluster_barrier();
+  }
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();

@@ -186,11 +186,28 @@ cudaError_t launch_dkv_pair(const BwdLaunch& a) {
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const TileOrder order = kv_block_order(a.s, C::D);
-  const int64_t grid = int64_t(2) * order.units * order.tiles;
+  const int64_t grid = int64_t(C::CLUSTER) * order.units * order.tiles;
   if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, a.stream>>>(
-      mq, mdo, a.k, a.v, a.lse, a.dvec, a.dk, a.dv, a.scale, a.s, order, a.wc);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C::CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mq, mdo, a.k, a.v, a.lse, static_cast<const float*>(a.dvec),
+                            a.dk, a.dv, a.scale, a.s, order, a.wc);
+}
+
+// D = 256 dK/dV: two pairs per KV block when the blocks fit twice over on the
+// SMs' pairs (so one causal block's query tiles are not the critical path alone).
+inline bool dkv_pair_halves(const AttnShape& s) {
+  return 4 * static_cast<int64_t>(s.B) * s.Hkv * ((s.Tkv + kBM - 1) / kBM) <= 2 * device_sm_count();
 }
 
 template <class C, class Kern>
@@ -278,7 +295,8 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
       else
         e = launch_dkv_with<C>(a, fa_bwd_dkv_kernel<C>);
     } else {
-      e = launch_dkv_pair<DkvPairCfg<BF16>>(a);
+      e = dkv_pair_halves(a.s) ? launch_dkv_pair<DkvPairCfg<BF16, 2>>(a)
+                               : launch_dkv_pair<DkvPairCfg<BF16>>(a);
     }
   }
   if (e != cudaSuccess) return e;
