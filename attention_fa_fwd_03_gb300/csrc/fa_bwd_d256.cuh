@@ -1,4 +1,5 @@
-// dK/dV for head dim 256 on a pair of CTAs (a thread-block cluster of two).
+// dK/dV for head dim 256 on a pair of CTAs (or two pairs of a four-CTA
+// cluster on small grids).
 //
 // What it computes is backward pass 2 of page "mlx-bun 0.0.4: package/src/
 // model/flash-attention.ts" with the KV-row ownership of page "[Metal] Add

@@ -172,8 +172,9 @@ inline bool dkv_small_grid(const AttnShape& s) {
          2 * static_cast<int64_t>(s.B) * s.Hkv * ((s.Tkv + kBM - 1) / kBM) <= device_sm_count();
 }
 
-// D = 256 dK/dV: one cluster of two CTAs per 128-row KV block
-// (fa_bwd_dkv_pair_kernel), non-persistent, heaviest blocks first.
+// D = 256 dK/dV: one cluster of C::CLUSTER CTAs (one or two pairs) per
+// 128-row KV block (fa_bwd_dkv_pair_kernel), non-persistent, heaviest blocks
+// first.
 template <class C>
 cudaError_t launch_dkv_pair(const BwdLaunch& a) {
   const int bhq = a.s.B * a.s.Hq;
@@ -237,9 +238,10 @@ constexpr int kSoftmaxWarpgroups = 4;
 
 // Backward for one head dim. D <= 128: the pipelined 128 x 128 kernels
 // (fa_bwd_pipelined.cuh). D = 256: the dK and dV accumulators alone fill TMEM,
-// so dV and dK are computed by the two CTAs of a cluster that exchange P
-// (fa_bwd_d256.cuh), and dQ runs the pipelined kernel with 64-key tiles and Q
-// in TMEM.
+// so dV and dK are computed by the two CTAs of a pair that exchange P (two
+// pairs per KV block on small grids; fa_bwd_d256.cuh), and dQ runs the
+// pipelined kernel with 64-key tiles and Q in TMEM. Tq <= 8: the vector dK/dV
+// and the split-key dQ (fa_decode.cuh).
 // dQ of short query blocks on the split-key kernel (defined below)
 template <int D, bool BF16>
 cudaError_t run_dq_decode(const BwdLaunch& a);

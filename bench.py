@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -114,14 +115,22 @@ COMMON_SOURCES = ["fa_common.cuh", "sm103_ptx.cuh", "fa_inst.cuh", "fa_inst_d64.
                   "fa_inst_d96.cu", "fa_inst_d128.cu", "fa_inst_d256.cu"]
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments, runs of whitespace collapsed (string
+    literals in these sources hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_digest(kernel: str) -> str:
-    """Digest of the sources that define ``kernel`` (its body, the shared
-    device helpers and the tile configurations)."""
+    """Digest of the code that defines ``kernel`` (its body, the shared device
+    helpers and the tile configurations), comments and layout excluded."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_fa_fwd_03_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel] + COMMON_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(name.encode() + fh.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as fh:
+            h.update(name.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
