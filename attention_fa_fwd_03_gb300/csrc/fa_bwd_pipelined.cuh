@@ -105,10 +105,11 @@ __device__ __forceinline__ DkvItem dkv_item(int linear, const TileOrder& o, cons
 }
 
 // SPLIT = 2: each work item's tiles are split between the two CTAs of a
-// cluster (for grids with fewer items than half the SMs); CTA 1 leaves its
-// fp32 dK / dV partial sums in its shared memory and CTA 0 adds them to its
-// own through distributed shared memory before it stores. One item per
-// cluster (no cluster launch control).
+// cluster (for grids with fewer items than half the SMs). Each CTA leaves in
+// its shared memory the fp32 partial sums of the half it does not finish
+// (CTA 0 its dK, CTA 1 its dV); after a cluster barrier CTA 0 adds CTA 1's dV
+// to its own and stores dV, CTA 1 adds CTA 0's dK and stores dK, each through
+// distributed shared memory. One item per cluster (no cluster launch control).
 template <int D_, bool BF16_, int NWG_, int SPLIT_ = 1>
 struct DkvCfg {
   static constexpr int D = D_;
@@ -157,9 +158,9 @@ struct DkvCfg {
   static constexpr uint32_t dst_col(int kk) { return chunk_operand_col(DP_COL, kk); }
   static_assert(NWG == 4, "one 32-column chunk per softmax warpgroup");
   static_assert(D <= 128, "dV and dK accumulators share 256 TMEM columns");
-  // CTA 1's partial sums: 128 rows x [dV | dK] fp32 over the tile buffers
+  // the half a CTA hands to its peer: 128 rows x D fp32 over the tile buffers
   // (free once the item's MMAs have completed), 16-byte chunks swizzled by row
-  static constexpr int PART_ROW = 2 * D * 4;
+  static constexpr int PART_ROW = D * 4;
   static_assert(SPLIT == 1 || (SPLIT == 2 && 128 * PART_ROW <= OFF_STATS &&
                                (PART_ROW / 16) % 8 == 0), "partial sums buffer");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -534,16 +535,17 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         tc_fence_after();
       }
       if constexpr (C::SPLIT > 1) {
-        // CTA 1: its partial sums to its own shared memory (the tile buffers
-        // are free: the item's MMAs have completed); CTA 0 adds them after the
-        // cluster barrier at the end
-        if (part == 1) {
+        // the half the peer finishes (CTA 0: dK, CTA 1: dV) to this CTA's own
+        // shared memory (the tile buffers are free: the item's MMAs have
+        // completed); the peer adds it after the cluster barrier at the end
+        {
           const int row = quarter * 32 + lane;
+          const uint32_t half = part == 0 ? C::DK_COL : C::DV_COL;
 #pragma unroll 1
-          for (int c = wg; c < C::PART_ROW / 64; c += C::NWG) {  // 16-column chunks
+          for (int c = wg; c < C::D / 16; c += C::NWG) {  // 16-column chunks
             uint32_t v[16];
             if (have) {
-              tmem_ld16(tmem + lane_base + C::DV_COL + 16 * c, v);
+              tmem_ld16(tmem + lane_base + half + 16 * c, v);
               tmem_ld_wait();
             } else {
 #pragma unroll
@@ -586,30 +588,34 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   }
 
   if constexpr (C::SPLIT > 1) {
-    // every thread of both CTAs: CTA 1's partial sums are in its shared memory
+    // every thread of both CTAs: each CTA's half for its peer is in its shared
+    // memory
     cluster_barrier();
-    if (part == 0 && warp >= 4 && !*abort_flag) {
-      // CTA 0: its accumulators plus CTA 1's partial sums, rounded and stored
-      // (dK scaled); 16-column chunks dealt over the softmax warpgroups
+    if (warp >= 4 && !*abort_flag) {
+      // CTA 0: dV, CTA 1: dK (scaled) — its own accumulator plus the peer's
+      // partial sums, rounded and stored; 16-column chunks dealt over the
+      // softmax warpgroups
       const DkvItem t = item_of(first_item);
       const int wg = (warp - 4) >> 2, quarter = warp & 3;
       const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
       const int row = quarter * 32 + lane, krow = t.k0 + row;
       const bool have = t.n_iter > 0;
       using T16 = typename std::conditional<C::BF16, __nv_bfloat16, __half>::type;
+      const bool is_dk = part == 1;
 #pragma unroll 1
-      for (int c = wg; c < C::PART_ROW / 64; c += C::NWG) {
+      for (int c = wg; c < C::D / 16; c += C::NWG) {
         uint32_t v[16];
         if (have) {
           tc_fence_after();
-          tmem_ld16(tmem + lane_base + C::DV_COL + 16 * c, v);
+          tmem_ld16(tmem + lane_base + (is_dk ? C::DK_COL : C::DV_COL) + 16 * c, v);
           tmem_ld_wait();
         }
         float x[16];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint4 w;
-          const uint32_t remote = peer_addr(sbase + row * C::PART_ROW + (((4 * c + q) ^ (row & 7)) << 4), 1);
+          const uint32_t remote =
+              peer_addr(sbase + row * C::PART_ROW + (((4 * c + q) ^ (row & 7)) << 4), part ^ 1);
           asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(remote));
           x[4 * q] = __uint_as_float(w.x);
@@ -617,7 +623,6 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           x[4 * q + 2] = __uint_as_float(w.z);
           x[4 * q + 3] = __uint_as_float(w.w);
         }
-        const bool is_dk = 16 * c >= C::D;
         const float mul = is_dk ? scale : 1.f;
         uint32_t o[8];
 #pragma unroll
@@ -628,13 +633,13 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
         if (krow < s.Tkv) {
           T16* dst = reinterpret_cast<T16*>(is_dk ? dk_out : dv_out) +
-                     (static_cast<int64_t>(t.bg) * s.Tkv + krow) * C::D + (is_dk ? 16 * c - C::D : 16 * c);
+                     (static_cast<int64_t>(t.bg) * s.Tkv + krow) * C::D + 16 * c;
           reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
           reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
       }
     }
-    // CTA 1 keeps its shared memory until CTA 0 has read it
+    // each CTA keeps its shared memory until the peer has read it
     cluster_barrier();
   }
 
