@@ -95,9 +95,13 @@ size_t fa_bwd_workspace_size(int B, int Hq, int Tq);
  * VJP for training", Implementation Notes: two kernels, KV-row ownership so
  * grouped heads reduce without atomics). Launches, in order on `stream`:
  *   1. D-vector preprocess  D = rowsum(dO o O)   (from the stored O)
- *   2. dK/dV kernel (one CTA owns a block of KV rows and loops over every
- *      query head of its group and every query tile that can see it)
- *   3. dQ kernel (one CTA owns a block of query rows, loops over KV tiles)
+ *   2. dK/dV kernel (one CTA, or a cluster of CTAs sharing the tiles, owns a
+ *      block of KV rows and loops over every query head of its group and
+ *      every query tile that can see it; Tq <= 8: a kernel that sums over
+ *      every query row of the group in fp32 per key row, any mask)
+ *   3. dQ kernel (one CTA owns a block of query rows, loops over KV tiles;
+ *      Tq <= 8: a split-key kernel over thread-block clusters of up to 8 CTAs)
+ * Which kernels run changes only the rounding order of the fp32 sums.
  *   q, k, v, o, dO, lse       inputs (o and lse as written by fa_fwd)
  *   dq [B,Hq,Tq,D], dk/dv [B,Hkv,Tkv,D]  outputs, dtype `dt`
  *   workspace                 caller-owned device scratch of at least
