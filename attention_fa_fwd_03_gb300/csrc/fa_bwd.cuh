@@ -27,6 +27,8 @@ fa_bwd_dvec_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
   constexpr int TPR = CHUNKS <= 8 ? 8 : (CHUNKS <= 16 ? 16 : 32);
   constexpr int ROWS_PER_BLOCK = 256 / TPR;
   constexpr int U = 4;  // rows per thread group per loop trip
+  grid_wait_prior();  // the previous grid's outputs are complete and visible
+  grid_release_next();
   const int sub = threadIdx.x % TPR;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * ROWS_PER_BLOCK;
   for (int64_t base = static_cast<int64_t>(blockIdx.x) * ROWS_PER_BLOCK; base < nrows;

@@ -136,7 +136,10 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
   if (threadIdx.x == 0) {
     *abort_flag = aligned ? 0 : 1;
     *peer_sent = 0;
-    if (!aligned) atomicOr(wc.status, kStatusSmemMisaligned);
+    if (!aligned) {
+      grid_wait_prior();
+      atomicOr(wc.status, kStatusSmemMisaligned);
+    }
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
       if (i == C::B_STFULL || i == C::B_STFULL + 1) cnt = 32;  // the staging warp's lanes
@@ -154,6 +157,8 @@ fa_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  grid_wait_prior();  // the previous grid's outputs are complete and visible
+  grid_release_next();
   tc_fence_before();
   __syncthreads();
   // every CTA has initialised its barriers before any arrives on a peer's or

@@ -179,6 +179,7 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
+    grid_wait_prior();
     if (threadIdx.x == 0) atomicOr(wc.status, kStatusSmemMisaligned);
     return;
   }
@@ -217,6 +218,8 @@ fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  grid_wait_prior();  // the previous grid's outputs are complete and visible
+  grid_release_next();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -769,10 +772,11 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                  const void* __restrict__ q_rows, const float* __restrict__ lse,
                  const float* __restrict__ dvec, void* __restrict__ dq_out, float scale,
-                 AttnShape s, TileOrder order, WaitCfg wc) {
+                 AttnShape s, TileOrder order, WaitCfg wc, int overlap_prior) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
+    grid_wait_prior();
     if (threadIdx.x == 0) atomicOr(wc.status, kStatusSmemMisaligned);
     return;
   }
@@ -800,6 +804,14 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  // overlap_prior: the previous grid is the dK/dV launch of the same backward,
+  // which reads nothing this grid writes and writes nothing it reads, and
+  // which this grid follows only once every CTA of it has passed its own wait
+  // for the D-vector. Then the grid starts at once, filling the SMs dK/dV
+  // leaves idle or frees, and waits for it at exit instead, so its completion
+  // still implies that of every grid before it.
+  if (!overlap_prior) grid_wait_prior();
+  grid_release_next();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1153,6 +1165,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constan
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (overlap_prior) grid_wait_prior();
 }
 
 }  // namespace fa

@@ -144,6 +144,8 @@ fa_fwd_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_con
   const int nstage = (kend - kbeg + C::SK - 1) / C::SK;
   const uint64_t tmo = wc.timeout_cycles;
   cluster_arrive_relaxed();  // waited for before the first store into a peer
+  grid_wait_prior();  // the previous grid's outputs are complete and visible
+  grid_release_next();
 
   // stage i: K and V rows [kbeg + i * SK, + SK) into slot i % STAGES
   auto issue = [&](int i) {
@@ -408,7 +410,7 @@ fa_bwd_dq_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                         const uint16_t* __restrict__ q, const uint16_t* __restrict__ dout,
                         const float* __restrict__ lse, const float* __restrict__ dvec,
                         uint16_t* __restrict__ dq, float scale, AttnShape s, int split,
-                        int k_first, int k_last, int keys_per_cta, WaitCfg wc) {
+                        int k_first, int k_last, int keys_per_cta, WaitCfg wc, int overlap_prior) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full;
   __shared__ int abort_flag;
@@ -429,6 +431,11 @@ fa_bwd_dq_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
   const int nstage = (kend - kbeg + C::SK - 1) / C::SK;
   const uint64_t tmo = wc.timeout_cycles;
   cluster_arrive_relaxed();  // waited for before the first store into a peer
+  // overlap_prior: the previous grid is the dK/dV launch of the same backward
+  // (it and this grid touch disjoint outputs and share only inputs complete
+  // before it passed its own wait): start at once, wait for it at exit
+  if (!overlap_prior) grid_wait_prior();
+  grid_release_next();
 
   auto issue = [&](int i) {
     const uint32_t bar = smem_u32(&full);
@@ -616,6 +623,7 @@ fa_bwd_dq_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         out[d] = __float2half_rn(x * scale);
     }
   }
+  if (overlap_prior) grid_wait_prior();
 }
 
 }  // namespace fa
@@ -699,6 +707,8 @@ fa_bwd_dkv_vec_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict
   for (int m = 0; m < C::NG; ++m)
 #pragma unroll
     for (int x = 0; x < 4; ++x) adk[m][x] = adv[m][x] = 0.f;
+  grid_wait_prior();  // the previous grid's outputs are complete and visible
+  grid_release_next();
   int kf, kl;
   key_range(s, 0, s.Tq, &kf, &kl);
   if (j0 < kl && j0 + kVecKeys > kf) {

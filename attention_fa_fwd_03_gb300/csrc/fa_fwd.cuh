@@ -90,18 +90,21 @@ struct FwdCfg {
   // tensor core to finish PV before its next scores exist.
   static constexpr int SBUF = NQ * (2 * BN + DP) <= 512 ? 2 : 1;
   // barriers: q_full, q_empty, k_full[S], v_full[S], k_empty[S], v_empty[S],
-  // s_full[NQ][SBUF], p_full[NQ][SBUF], o_ready[NQ], drain, item responses
+  // s_full[NQ][SBUF], p_full[NQ][SBUF], o_ready[NQ][2], drain, item responses
   // full / empty. p_full has one barrier per score buffer: with two buffers a
   // softmax warp can finish tile j+1 while a sibling still works on tile j,
-  // and its arrival must not count towards tile j.
+  // and its arrival must not count towards tile j. o_ready has one barrier per
+  // key-tile parity (PV(j) completes phase j / 2 of o_ready[j % 2]), so each
+  // advances once every two tiles and a waiter is never two phases off.
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = B_KFULL + STAGES,
                        B_KEMPTY = B_VFULL + STAGES, B_VEMPTY = B_KEMPTY + STAGES,
                        B_SFULL = B_VEMPTY + STAGES, B_PFULL = B_SFULL + NQ * SBUF,
-                       B_OREADY = B_PFULL + NQ * SBUF, B_DRAIN = B_OREADY + NQ,
+                       B_OREADY = B_PFULL + NQ * SBUF, B_DRAIN = B_OREADY + 2 * NQ,
                        B_CLCFULL = B_DRAIN + 1, B_CLCEMPTY = B_CLCFULL + kClcSlots,
                        NBAR = B_CLCEMPTY + kClcSlots;
   static constexpr int sfull(int t, int b) { return B_SFULL + t * SBUF + b; }
   static constexpr int pfull(int t, int b) { return B_PFULL + t * SBUF + b; }
+  static constexpr int oready(int t, int j) { return B_OREADY + 2 * t + (j & 1); }
   static constexpr int OFF_CLC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;
   static constexpr int OFF_MISC = OFF_CLC + 16 * kClcSlots;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -157,6 +160,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
+  grid_wait_prior();  // the previous grid's outputs are complete and visible
+  grid_release_next();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -297,7 +302,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             if (!ok) break;
             tc_fence_after();
             if (leader) issue_pv(tq, st, b, it > 0);
-            if (leader) mma_commit(bar(C::B_OREADY + tq));
+            if (leader) mma_commit(bar(C::oready(tq, gi)));
             if (next) {
               if (leader) issue_s(tq, nst, b);  // after PV(gi) read P from buffer b
               if (leader) mma_commit(bar(C::sfull(tq, b)));
@@ -397,10 +402,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const float rs = (a01.x + a01.y) + (a23.x + a23.y);
         l = l * alpha + rs;
         if (it > 0 && __any_sync(0xffffffffu, grow)) {
-          // O_t holds the sum of the previous tiles: wait for the last of them
-          // (PV(gi-2) has completed: S(gi), just read, was issued after it, so
-          // the barrier is at most one phase behind).
-          ok = mbar_wait(bar(C::B_OREADY + tq), (gi - 1) & 1, tmo, abort_flag, wc.status);
+          // O_t holds the sum of the previous tiles: wait for the last of them,
+          // PV(gi-1). Its barrier's previous phase, PV(gi-3), has completed
+          // (S(gi), just read, was issued after PV(gi-2)), and its next, PV(gi+1),
+          // waits for this warp's P: at most one phase off.
+          ok = mbar_wait(bar(C::oready(tq, gi - 1)), ((gi - 1) >> 1) & 1, tmo, abort_flag,
+                         wc.status);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -427,19 +434,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       // P, which comes after these reads.
       const bool have = t.n_iter > 0;
       if (have) {
-        // O_t is final once the block's last PV completed. A parity wait is
-        // only sound when the barrier is at most one phase off. Behind: with
-        // two score buffers the block's last S was issued before its
-        // second-to-last PV, which may still be running, so that PV is waited
-        // for first. Ahead: the last PV is issued only after the MMA warp has
-        // seen this warp's arrival just above and runs for 512 cycles or more,
-        // while this warp reaches the wait within a few ALU instructions. (A
-        // per-block barrier committed by the MMA warp would close this by
-        // construction; measured, it cost the forward 4-7%.)
+        // O_t is final once the block's last PV completed (its commit also
+        // covers every MMA issued before it). A parity wait is sound only while
+        // the barrier is at most one phase off, which holds by construction:
+        // PV(last) shares its barrier with PV(last-2), complete since S(last)
+        // was issued after it, and PV(last+2), which needs this warp's next P.
+        // (A single barrier for all PVs, waited for PV(last-1) and then
+        // PV(last), could be two phases past the first wait when this warp ran
+        // late, and that wait then never ended.)
         const int last = gk + t.n_iter - 1;
-        if (C::SBUF == 2 && t.n_iter > 1)
-          ok = mbar_wait(bar(C::B_OREADY + tq), (last - 1) & 1, tmo, abort_flag, wc.status);
-        ok = ok && mbar_wait(bar(C::B_OREADY + tq), last & 1, tmo, abort_flag, wc.status);
+        ok = mbar_wait(bar(C::oready(tq, last)), (last >> 1) & 1, tmo, abort_flag, wc.status);
         if (!ok) break;
         tc_fence_after();
       }

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <atomic>
 #include <type_traits>
+#include <utility>
 
 #include "fa_bwd.cuh"
 #include "fa_bwd_d256.cuh"
@@ -15,6 +16,39 @@
 #include "fa_launch.h"
 
 namespace fa {
+
+// Every kernel is launched with programmatic stream serialisation: its launch
+// and prologue overlap the end of the previous kernel in the stream, and it
+// waits for that kernel (grid_wait_prior) before it touches global memory.
+// Appends the attribute to cfg's attribute array `attrs`, which must have room.
+inline void allow_early_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attrs) {
+  cudaLaunchAttribute& at = attrs[cfg->numAttrs++];
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  cfg->attrs = attrs;
+}
+
+// Launches kern on a 1-D grid of `grid` CTAs (in clusters of `cluster`).
+template <class... P, class... A>
+cudaError_t launch_kernel(void (*kern)(P...), int64_t grid, int threads, int smem,
+                          cudaStream_t stream, unsigned cluster, A&&... args) {
+  if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  if (cluster > 1) {
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = cluster;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    cfg.numAttrs = 1;
+  }
+  allow_early_launch(&cfg, attrs);
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
+}
 
 // A kernel that moves registers between its warpgroups (setmaxnreg) may only
 // be launched when its launch-time registers cover the new counts; otherwise
@@ -80,9 +114,8 @@ cudaError_t run_fwd(const FwdLaunch& a) {
   if (!register_split_fits(reinterpret_cast<const void*>(kern), C::THREADS, C::REG_NEEDED))
     return cudaErrorInvalidConfiguration;
   const TileOrder order = query_block_order(a.s, C::NQ * kBM, C::D);
-  kern<<<order.units * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, a.o, a.lse,
-                                                                           a.s, order, a.wc);
-  return cudaGetLastError();
+  return launch_kernel(kern, int64_t(order.units) * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream,
+                       1, mq, mk, mv, a.o, a.lse, a.s, order, a.wc);
 }
 
 template <int D, bool BF16>
@@ -94,9 +127,9 @@ cudaError_t run_dvec(const BwdLaunch& a) {
   const int64_t want = (nrows + rows_per_block - 1) / rows_per_block;
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
   const int blocks = static_cast<int>(want < cap ? want : cap);
-  fa_bwd_dvec_kernel<D, BF16><<<blocks, 256, 0, a.stream>>>(
-      static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.dvec, nrows);
-  return cudaGetLastError();
+  return launch_kernel(fa_bwd_dvec_kernel<D, BF16>, blocks, 256, 0, a.stream, 1,
+                       static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.dvec,
+                       nrows);
 }
 
 // Kernel configurations without a register split need no check.
@@ -124,9 +157,8 @@ cudaError_t launch_dkv_with(const BwdLaunch& a, Kern kern) {
   if (!register_split_fits(reinterpret_cast<const void*>(kern), C::THREADS, RegSplit<C>::needed))
     return cudaErrorInvalidConfiguration;
   const TileOrder order = kv_block_order(a.s, C::D);
-  kern<<<order.units * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream>>>(
-      mq, mk, mv, mdo, a.lse, a.dvec, a.dk, a.dv, a.scale, a.s, order, a.wc);
-  return cudaGetLastError();
+  return launch_kernel(kern, int64_t(order.units) * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream,
+                       1, mq, mk, mv, mdo, a.lse, a.dvec, a.dk, a.dv, a.scale, a.s, order, a.wc);
 }
 
 // dK/dV with each item's tiles split over the two CTAs of a cluster (one item
@@ -146,20 +178,9 @@ cudaError_t launch_dkv_split(const BwdLaunch& a) {
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const TileOrder order = kv_block_order(a.s, C::D);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(C::SPLIT * order.units * order.tiles), 1, 1);
-  cfg.blockDim = dim3(C::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C::SPLIT;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, a.lse, static_cast<const float*>(a.dvec),
-                            a.dk, a.dv, a.scale, a.s, order, a.wc);
+  return launch_kernel(kern, int64_t(C::SPLIT) * order.units * order.tiles, C::THREADS,
+                       C::SMEM_BYTES, a.stream, C::SPLIT, mq, mk, mv, mdo, a.lse,
+                       static_cast<const float*>(a.dvec), a.dk, a.dv, a.scale, a.s, order, a.wc);
 }
 
 // Split each KV block's query tiles over a two-CTA cluster when the blocks
@@ -187,22 +208,9 @@ cudaError_t launch_dkv_pair(const BwdLaunch& a) {
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const TileOrder order = kv_block_order(a.s, C::D);
-  const int64_t grid = int64_t(C::CLUSTER) * order.units * order.tiles;
-  if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(C::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C::CLUSTER;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, mq, mdo, a.k, a.v, a.lse, static_cast<const float*>(a.dvec),
-                            a.dk, a.dv, a.scale, a.s, order, a.wc);
+  return launch_kernel(kern, int64_t(C::CLUSTER) * order.units * order.tiles, C::THREADS,
+                       C::SMEM_BYTES, a.stream, C::CLUSTER, mq, mdo, a.k, a.v, a.lse,
+                       static_cast<const float*>(a.dvec), a.dk, a.dv, a.scale, a.s, order, a.wc);
 }
 
 // D = 256 dK/dV: two pairs per KV block when the blocks fit twice over on the
@@ -211,8 +219,10 @@ inline bool dkv_pair_halves(const AttnShape& s) {
   return 4 * static_cast<int64_t>(s.B) * s.Hkv * ((s.Tkv + kBM - 1) / kBM) <= 2 * device_sm_count();
 }
 
+// overlap_prior: the dK/dV launch of the same backward directly precedes this
+// one on the stream (see fa_bwd_dq_kernel).
 template <class C, class Kern>
-cudaError_t launch_dq_with(const BwdLaunch& a, Kern kern) {
+cudaError_t launch_dq_with(const BwdLaunch& a, Kern kern, bool overlap_prior) {
   const int bhq = a.s.B * a.s.Hq, bhkv = a.s.B * a.s.Hkv;
   CUtensorMap mq, mk, mv, mdo;
   if (!encode_tile_map(&mq, a.q, C::BF16, C::D, a.s.Tq, bhq, kBM) ||
@@ -226,9 +236,9 @@ cudaError_t launch_dq_with(const BwdLaunch& a, Kern kern) {
   if (!register_split_fits(reinterpret_cast<const void*>(kern), C::THREADS, RegSplit<C>::needed))
     return cudaErrorInvalidConfiguration;
   const TileOrder order = query_block_order(a.s, kBM, C::D);
-  kern<<<order.units * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream>>>(
-      mq, mk, mv, mdo, a.q, a.lse, a.dvec, a.dq, a.scale, a.s, order, a.wc);
-  return cudaGetLastError();
+  return launch_kernel(kern, int64_t(order.units) * order.tiles, C::THREADS, C::SMEM_BYTES, a.stream,
+                       1, mq, mk, mv, mdo, a.q, a.lse, a.dvec, a.dq, a.scale, a.s, order, a.wc,
+                       overlap_prior ? 1 : 0);
 }
 
 // Softmax warpgroups of the pipelined backward kernels: four (32 score columns
@@ -244,7 +254,7 @@ constexpr int kSoftmaxWarpgroups = 4;
 // and the split-key dQ (fa_decode.cuh).
 // dQ of short query blocks on the split-key kernel (defined below)
 template <int D, bool BF16>
-cudaError_t run_dq_decode(const BwdLaunch& a);
+cudaError_t run_dq_decode(const BwdLaunch& a, bool overlap_prior);
 
 // dK / dV of short query blocks: the vector kernel, one CTA per (batch, KV
 // group, kVecKeys keys), on the call's own row shape, in chunks of RC rows.
@@ -258,11 +268,10 @@ cudaError_t launch_dkv_vec(const BwdLaunch& a) {
   const int64_t blocks =
       static_cast<int64_t>(s.B) * s.Hkv * ((s.Tkv + kVecKeys - 1) / kVecKeys);
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), kVecThreads, C::SMEM_BYTES, a.stream>>>(
-      static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k),
-      static_cast<const uint16_t*>(a.v), static_cast<const uint16_t*>(a.dout), a.lse, a.dvec,
-      static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), s);
-  return cudaGetLastError();
+  return launch_kernel(kern, blocks, kVecThreads, C::SMEM_BYTES, a.stream, 1,
+                       static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k),
+                       static_cast<const uint16_t*>(a.v), static_cast<const uint16_t*>(a.dout),
+                       a.lse, a.dvec, static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), s);
 }
 
 template <int D, bool BF16>
@@ -281,6 +290,18 @@ cudaError_t run_dkv_vec(const BwdLaunch& a) {
 // one tile, and 12.4 against 19.9 us for a causal Tq = 8 call on one tile per
 // head.
 inline bool dkv_vector_path(const BwdLaunch& a) { return a.s_rows.Tq <= kDecodeMaxTq; }
+
+// dQ starts beside dK/dV (fa_bwd_dq_kernel's overlap_prior) where dK/dV leaves
+// SMs idle for long: masked grids, whose KV blocks carry unequal numbers of
+// tiles so the SMs run dry one by one, and short query blocks, whose small
+// vector and split-key CTAs share SMs. Unmasked tile grids finish their equal
+// blocks together; there the dQ CTAs that start early only take a second
+// block each while the rest start late, which measured slower (B2 Hq8 Hkv8
+// T1024 D128: 62.2 against 58.2 us per fwd + bwd step; causal B2 Hq8 Hkv2
+// T2048 D64: 80.5 against 104.7).
+inline bool dq_overlaps_dkv(const BwdLaunch& a) {
+  return a.s_rows.causal != 0 || a.s_rows.window > 0 || dkv_vector_path(a);
+}
 
 template <int D, bool BF16>
 cudaError_t run_bwd(const BwdLaunch& a, int phases) {
@@ -303,14 +324,17 @@ cudaError_t run_bwd(const BwdLaunch& a, int phases) {
   }
   if (e != cudaSuccess) return e;
   if (phases & kPhaseDq) {
-    if (a.s_rows.Tq <= kDecodeMaxTq) return run_dq_decode<D, BF16>(a);
+    // dQ needs only the D-vector of the phases before it: right after this
+    // call's dK/dV launch it may start without waiting for that grid
+    const bool overlap = (phases & kPhaseDkv) != 0 && dq_overlaps_dkv(a);
+    if (a.s_rows.Tq <= kDecodeMaxTq) return run_dq_decode<D, BF16>(a, overlap);
     if constexpr (D <= 128) {
       using C = DqCfg<D, BF16, kSoftmaxWarpgroups>;
-      e = launch_dq_with<C>(a, fa_bwd_dq_kernel<C>);
+      e = launch_dq_with<C>(a, fa_bwd_dq_kernel<C>, overlap);
     } else {
       // 64-key tiles, two softmax warpgroups, Q in TMEM, K / V rings 3 / 2
       using C = DqCfg<D, BF16, 2, 64, 3, 2, true>;
-      e = launch_dq_with<C>(a, fa_bwd_dq_kernel<C>);
+      e = launch_dq_with<C>(a, fa_bwd_dq_kernel<C>, overlap);
     }
   }
   return e;
@@ -391,12 +415,13 @@ cudaError_t launch_fwd_decode(const FwdLaunch& a) {
       !encode_tile_map(&mv, a.v, C::BF16, C::D, a.s.Tkv, bhkv, C::SK))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   decode_config(&cfg, attr, C::SMEM_BYTES, a.stream);
   static std::atomic<int> max_active[64][kDecodeMaxSplit + 1] = {};  // shared by host threads
   int split, per;
   decode_split(reinterpret_cast<const void*>(kern), &cfg, attr, max_active,
                static_cast<int64_t>(a.s.B) * a.s.Hq, k_last - k_first, &split, &per);
+  allow_early_launch(&cfg, attr);
   return cudaLaunchKernelEx(&cfg, kern, mk, mv, static_cast<const uint16_t*>(a.q),
                             static_cast<uint16_t*>(a.o), a.lse, a.s, split, k_first, k_last, per,
                             a.wc);
@@ -405,7 +430,7 @@ cudaError_t launch_fwd_decode(const FwdLaunch& a) {
 // dQ of short query blocks, on the call's own (unfolded) shape; reads the
 // D-vector the first backward phase wrote.
 template <class C>
-cudaError_t launch_dq_decode(const BwdLaunch& a) {
+cudaError_t launch_dq_decode(const BwdLaunch& a, bool overlap_prior) {
   const AttnShape& s = a.s_rows;
   int k_first, k_last;
   key_range(s, 0, s.Tq, &k_first, &k_last);
@@ -419,25 +444,26 @@ cudaError_t launch_dq_decode(const BwdLaunch& a) {
       !encode_tile_map(&mv, a.v, C::BF16, C::D, s.Tkv, bhkv, C::SK))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   decode_config(&cfg, attr, C::SMEM_BYTES, a.stream);
   static std::atomic<int> max_active[64][kDecodeMaxSplit + 1] = {};  // shared by host threads
   int split, per;
   decode_split(reinterpret_cast<const void*>(kern), &cfg, attr, max_active,
                static_cast<int64_t>(s.B) * s.Hq, k_last - k_first, &split, &per);
+  allow_early_launch(&cfg, attr);
   return cudaLaunchKernelEx(&cfg, kern, mk, mv, static_cast<const uint16_t*>(a.q),
                             static_cast<const uint16_t*>(a.dout), a.lse, a.dvec,
                             static_cast<uint16_t*>(a.dq), a.scale, s, split, k_first, k_last, per,
-                            a.wc);
+                            a.wc, overlap_prior ? 1 : 0);
 }
 
 template <int D, bool BF16>
-cudaError_t run_dq_decode(const BwdLaunch& a) {
+cudaError_t run_dq_decode(const BwdLaunch& a, bool overlap_prior) {
   const int tq = a.s_rows.Tq;
-  if (tq <= 1) return launch_dq_decode<DecodeDqCfg<D, 1, BF16>>(a);
-  if (tq <= 2) return launch_dq_decode<DecodeDqCfg<D, 2, BF16>>(a);
-  if (tq <= 4) return launch_dq_decode<DecodeDqCfg<D, 4, BF16>>(a);
-  return launch_dq_decode<DecodeDqCfg<D, 8, BF16>>(a);
+  if (tq <= 1) return launch_dq_decode<DecodeDqCfg<D, 1, BF16>>(a, overlap_prior);
+  if (tq <= 2) return launch_dq_decode<DecodeDqCfg<D, 2, BF16>>(a, overlap_prior);
+  if (tq <= 4) return launch_dq_decode<DecodeDqCfg<D, 4, BF16>>(a, overlap_prior);
+  return launch_dq_decode<DecodeDqCfg<D, 8, BF16>>(a, overlap_prior);
 }
 
 template <int D, bool BF16>

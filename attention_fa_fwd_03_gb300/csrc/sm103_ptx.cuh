@@ -40,6 +40,24 @@ __device__ __forceinline__ bool elect_one_sync() {
   return pred != 0;
 }
 
+// -------------------------------------------- programmatic dependent launch
+// Every kernel is launched with programmatic stream serialisation: the grid
+// may be scheduled while the previous grid in the stream is still finishing.
+// Each thread calls grid_wait_prior() after its prologue (barrier set-up and
+// TMEM allocation, which touch no global memory) and before its first global
+// load or store, and before it can exit; it returns once the previous grid has
+// completed and its writes are visible (at once without such a dependency).
+// So a grid's completion still implies that of every grid before it.
+// grid_release_next() then lets the next grid be scheduled on the SMs this
+// one frees; it only ever waits on this grid, never the reverse.
+__device__ __forceinline__ void grid_wait_prior() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_release_next() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));

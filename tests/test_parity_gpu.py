@@ -334,13 +334,15 @@ def test_full_size_runs_repeat_bit_for_bit():
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,Tq,Tkv,D,dt,causal,window", [
-    (1, 4, 2, 300, 300, 128, "bf16", True, 0),       # tile kernels
-    (2, 8, 2, 4, 700, 128, "fp16", False, 0),        # short queries: folded dK/dV, split-key dQ
+    (1, 4, 2, 300, 300, 128, "bf16", True, 0),       # tile kernels, dQ beside dK/dV
+    (2, 4, 2, 260, 260, 64, "fp16", False, 0),       # tile kernels, dQ after dK/dV
+    (2, 8, 2, 4, 700, 128, "fp16", False, 0),        # short queries: vector dK/dV, split-key dQ
     (1, 2, 1, 200, 200, 256, "bf16", True, 64),      # D = 256 kernels
 ])
 def test_phase_calls_equal_fa_bwd(B, Hq, Hkv, Tq, Tkv, D, dt, causal, window):
     """fa_bwd_preprocess + fa_bwd_dkv + fa_bwd_dq (the phases the benchmark
-    times one by one) give exactly what one fa_bwd call gives."""
+    times one by one, each waiting for the one before) give exactly what one
+    fa_bwd call gives, where dQ may run beside dK/dV."""
     m = fa()
     w = fa_inputs.Workload("phases", B, Hq, Hkv, Tq, Tkv, D, dt, causal, window, seed=55)
     x = fa_inputs.make_inputs(w)
@@ -361,3 +363,44 @@ def test_phase_calls_equal_fa_bwd(B, Hq, Hkv, Tq, Tkv, D, dt, causal, window):
     assert m.fa_device_status() == 0
     for name, a, b in (("dq", one[0], dq), ("dk", one[1], dk), ("dv", one[2], dv)):
         assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,T,D,dt,causal,window", [
+    (2, 8, 2, 2048, 64, "fp16", True, 0),    # dQ starts beside dK/dV
+    (1, 8, 2, 8, 128, "bf16", False, 0),     # short queries: vector dK/dV beside split-key dQ
+    (2, 8, 8, 1024, 128, "bf16", False, 0),  # dQ after dK/dV
+])
+def test_stream_order_after_backward(B, Hq, Hkv, T, D, dt, causal, window):
+    """Kernels start while the previous one in the stream finishes, and dQ may
+    run beside dK/dV; work queued after fa_bwd on the same stream must still
+    see the whole backward done. Right after fa_bwd (no synchronisation) a
+    forward on other inputs overwrites O and the LSE the backward reads, and
+    stream-ordered copies take dQ, dK and dV: all must equal a backward run
+    alone."""
+    m = fa()
+    Tq, Tkv = T, (T if T > 8 else 1500)  # short queries read a longer key range
+    w = fa_inputs.Workload("order", B, Hq, Hkv, Tq, Tkv, D, dt, causal, window, seed=77)
+    x = fa_inputs.make_inputs(w)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    q2 = torch.flip(q, dims=[2]).contiguous()
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    ws = torch.empty(m.fa_bwd_workspace_size(B, Hq, Tq), dtype=torch.uint8, device=dev)
+    m.fa_fwd(q, k, v, o, lse, w.scale, causal, window)
+    o_keep, lse_keep = o.clone(), lse.clone()
+    ref = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+    m.fa_bwd(q, k, v, o, do, lse, *ref, w.scale, causal, window, workspace=ws)
+    torch.cuda.synchronize()
+    for _ in range(5):
+        o.copy_(o_keep)
+        lse.copy_(lse_keep)
+        got = [torch.full_like(t, float("nan")) for t in ref]
+        m.fa_bwd(q, k, v, o, do, lse, *got, w.scale, causal, window, workspace=ws)
+        m.fa_fwd(q2, k, v, o, lse, w.scale, causal, window)
+        copies = [t.clone() for t in got]
+        torch.cuda.synchronize()
+        assert m.fa_device_status() == 0
+        for name, a, b, c in zip(("dq", "dk", "dv"), ref, got, copies):
+            assert torch.equal(a, b), name
+            assert torch.equal(a, c), name + " (stream-ordered copy)"
