@@ -193,21 +193,32 @@ class ClockSampler:
     @staticmethod
     def parse(out: str, t0: float, t1: float) -> dict:
         import datetime
-        sm, mx, pw, reasons, outside = [], [], [], set(), 0
+        rows = []
         for line in out.splitlines():
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 10:
                 continue
             try:
                 ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                clk, clk_max = float(parts[2]), float(parts[3])
+                rows.append((ts, float(parts[2]), float(parts[3]), parts))
             except ValueError:
                 continue
-            if not (t0 <= ts <= t1):
-                outside += 1
-                continue
-            sm.append(clk)
-            mx.append(clk_max)
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        nearest = False
+        if not inside:
+            # a region shorter than the sampling interval: the samples just
+            # before and after it (within 0.1 s), marked as such
+            before = [r for r in rows if t0 - 0.1 <= r[0] < t0][-1:]
+            after = [r for r in rows if t1 < r[0] <= t1 + 0.1][:1]
+            inside, nearest = before + after, True
+        if not inside:
+            return {"error": "no clock sample inside the timed region",
+                    "samples_outside": len(rows)}
+        sm = [r[1] for r in inside]
+        mx = [r[2] for r in inside]
+        pw, reasons = [], set()
+        for r in inside:
+            parts = r[3]
             try:
                 pw.append(float(parts[4]))
             except ValueError:
@@ -215,10 +226,10 @@ class ClockSampler:
             for name, val in zip(ClockSampler.NAMES, parts[6:10]):
                 if val.lower() == "active":
                     reasons.add(name)
-        if not sm:
-            return {"error": "no clock sample inside the timed region", "samples_outside": outside}
         r = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "sm_min_mhz": min(sm),
              "samples": len(sm), "reasons": sorted(reasons)}
+        if nearest:
+            r["nearest_samples"] = "region shorter than the 50 ms sampling interval"
         if pw:
             r["power_w_median"] = statistics.median(pw)
         return r

@@ -73,3 +73,7 @@ def test_clock_sampler_keeps_only_samples_inside_the_timed_region():
     assert r["samples"] == 3 and r["sm_mhz"] == 1850.0 and r["sm_min_mhz"] == 1800.0
     assert r["reasons"] == ["sw_power_cap"]              # the hw_slowdown sample was outside
     assert "error" in bench.ClockSampler.parse(out, t0 + 5, t0 + 6)
+    # a region between two samples takes the one just before and the one just after it
+    r = bench.ClockSampler.parse(out, t0 + 0.21, t0 + 0.25)
+    assert r["samples"] == 2 and r["sm_min_mhz"] == 1800.0 and r["sm_max_mhz"] == 2070.0
+    assert "nearest_samples" in r and r["reasons"] == []

@@ -404,3 +404,38 @@ def test_stream_order_after_backward(B, Hq, Hkv, T, D, dt, causal, window):
         for name, a, b, c in zip(("dq", "dk", "dv"), ref, got, copies):
             assert torch.equal(a, b), name
             assert torch.equal(a, c), name + " (stream-ordered copy)"
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,T,D,dt,causal", [
+    (2, 8, 2, 2048, 64, "fp16", True),      # one query tile per CTA, two score buffers
+    (2, 8, 8, 1024, 128, "bf16", False),    # the same at D = 128
+    (2, 8, 2, 2048, 256, "fp16", True),     # D = 256: 64-key tiles, two score buffers
+])
+def test_two_buffer_forward_repeats_bitwise(B, Hq, Hkv, T, D, dt, causal):
+    """Forward configurations with two score buffers per query tile, run
+    back to back many times with each kernel launched while the previous one
+    finishes: every run bitwise equal to the first and no bounded wait gives
+    up. (A late softmax warp once found the forward's single O-ready barrier
+    two phases past its wait, which then never ended.)"""
+    m = fa()
+    w = fa_inputs.Workload("rep", B, Hq, Hkv, T, T, D, dt, causal, 0, seed=91)
+    x = fa_inputs.make_inputs(w)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(m.fa_bwd_workspace_size(B, Hq, T), dtype=torch.uint8, device=dev)
+    m.fa_device_status(clear=True)
+    runs = []
+    for r in range(100):
+        m.fa_fwd(q, k, v, o, lse, w.scale, causal, 0)
+        m.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.scale, causal, 0, workspace=ws)
+        if r % 25 == 0 or r == 99:  # copies on the stream; the runs between chain directly
+            runs.append([t.clone() for t in (o, lse, dq, dk, dv)])
+    torch.cuda.synchronize()
+    assert m.fa_device_status() == 0, "a bounded device wait gave up"
+    for got in runs[1:]:
+        for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), runs[0], got):
+            assert torch.equal(a, b), name
+    assert bool(torch.isfinite(runs[0][0]).all())
