@@ -413,14 +413,18 @@ def run_ours(args, rank, world, local_rank):
 
     sampler = ClockSampler(physical_gpu_index(local_rank))
     sampler.start()
-    time.sleep(0.25)  # let the sampler start before the timed regions
-    # the per-kernel region first, short (at most 100 steps), so the kernels
-    # are timed at the clock a burst runs at, as the burst peak was measured:
-    # the same step as phase calls (kernel times, roofline)
-    kernel_steps = min(args.steps, 100)
-    pevs, pwall, pwin = region(step_phases, 5, kernel_steps)
+    # Each region starts after a short idle: measured, the first region after
+    # one runs 3-5% faster than one that follows another region directly
+    # (same sampled clock), so neither region inherits the other's load.
+    time.sleep(0.25)
     # the timed region: the step through the public API (the line's value)
     evs, wall, win = region(step_api, 2, args.steps)
+    time.sleep(0.25)
+    # the per-kernel region, short (at most 100 steps, so its kernels run at
+    # the clock of a burst, as the burst peak was measured): the same step as
+    # phase calls (kernel times, roofline)
+    kernel_steps = min(args.steps, 100)
+    pevs, pwall, pwin = region(step_phases, 5, kernel_steps)
     if world > 1:
         torch.distributed.barrier()
     clocks, kernel_clocks = sampler.stop(win, pwin)
@@ -592,8 +596,9 @@ def run_ours(args, rank, world, local_rank):
         "kernels": kernels,
         "kernels_region": {"steps": kernel_steps, "clocks": kernel_clocks,
                            "what": ("the same step as the four phase calls with an event between "
-                                    "launches (which serialises them), just before the timed "
-                                    "region; fwd_ms, bwd_ms, kernels and the roofline come from it")},
+                                    "launches (which serialises them), after the timed region and "
+                                    "a 0.25 s idle; fwd_ms, bwd_ms, kernels and the roofline come "
+                                    "from it")},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
