@@ -81,6 +81,10 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
  * that launches thread-block clusters of up to 8 CTAs; longer query blocks run
  * the tensor-core tile kernel. Both compute the same result; which one runs
  * changes only the rounding of the fp32 sums.
+ * The kernel is launched with programmatic stream serialisation: its launch
+ * and set-up overlap the end of the previous kernel in `stream`, and it
+ * waits for that kernel to complete before it reads or writes global memory.
+ * So stream order is what the caller sees.
  * Returns FA_OK or an error code (nothing launched on error). */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int Hq, int Hkv, int Tq, int Tkv, int D, float scale,
@@ -102,6 +106,13 @@ size_t fa_bwd_workspace_size(int B, int Hq, int Tq);
  *   3. dQ kernel (one CTA owns a block of query rows, loops over KV tiles;
  *      Tq <= 8: a split-key kernel over thread-block clusters of up to 8 CTAs)
  * Which kernels run changes only the rounding order of the fp32 sums.
+ * Ordering: as for fa_fwd, each kernel is launched to overlap the end of the
+ * previous kernel in `stream` (programmatic stream serialisation). It waits
+ * for that kernel before it reads or writes global memory, so stream order
+ * holds for the caller. On causal, windowed and Tq <= 8 calls, the dQ kernel
+ * starts without waiting for the dK/dV kernel: it needs only the D-vector.
+ * It waits for dK/dV before it completes, so work queued after fa_bwd on
+ * `stream` still sees all three outputs written.
  *   q, k, v, o, dO, lse       inputs (o and lse as written by fa_fwd)
  *   dq [B,Hq,Tq,D], dk/dv [B,Hkv,Tkv,D]  outputs, dtype `dt`
  *   workspace                 caller-owned device scratch of at least
