@@ -338,6 +338,8 @@ def test_full_size_runs_repeat_bit_for_bit():
     (2, 4, 2, 260, 260, 64, "fp16", False, 0),       # tile kernels, dQ after dK/dV
     (2, 8, 2, 4, 700, 128, "fp16", False, 0),        # short queries: vector dK/dV, split-key dQ
     (1, 2, 1, 200, 200, 256, "bf16", True, 64),      # D = 256 kernels
+    (1, 6, 2, 400, 400, 96, "bf16", False, 150),     # window without causal: dQ beside dK/dV
+    (2, 8, 2, 6, 900, 64, "fp16", True, 0),          # causal short queries: vector dK/dV
 ])
 def test_phase_calls_equal_fa_bwd(B, Hq, Hkv, Tq, Tkv, D, dt, causal, window):
     """fa_bwd_preprocess + fa_bwd_dkv + fa_bwd_dq (the phases the benchmark
@@ -439,3 +441,53 @@ def test_two_buffer_forward_repeats_bitwise(B, Hq, Hkv, T, D, dt, causal):
         for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), runs[0], got):
             assert torch.equal(a, b), name
     assert bool(torch.isfinite(runs[0][0]).all())
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tq,Tkv,D,dt,causal,window", [
+    (2, 8, 2, 1024, 1024, 128, "bf16", True, 0),     # tile kernels, dQ beside dK/dV
+    (2, 4, 4, 640, 640, 64, "fp16", False, 0),       # tile kernels, dQ after dK/dV
+    (2, 8, 2, 4, 1000, 128, "fp16", False, 0),       # short queries
+    (1, 4, 2, 300, 300, 256, "bf16", True, 0),       # D = 256
+])
+def test_cuda_graph_capture_and_replay(B, Hq, Hkv, Tq, Tkv, D, dt, causal, window):
+    """fa_fwd + fa_bwd captured into a CUDA graph (consecutive kernels become
+    programmatic edges) and replayed on new inputs copied into the captured
+    buffers: bitwise what the same calls give outside the graph."""
+    m = fa()
+    w = fa_inputs.Workload("graph", B, Hq, Hkv, Tq, Tkv, D, dt, causal, window, seed=61)
+    x = fa_inputs.make_inputs(w)
+    x2 = fa_inputs.make_inputs(fa_inputs.Workload("graph2", B, Hq, Hkv, Tq, Tkv, D, dt, causal,
+                                                  window, seed=62))
+    dev = torch.device("cuda")
+    bufs = {n: x[n].to(dev) for n in ("q", "k", "v", "do")}
+    q, k, v, do = (bufs[n] for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(m.fa_bwd_workspace_size(B, Hq, Tq), dtype=torch.uint8, device=dev)
+
+    def step(stream=None):
+        m.fa_fwd(q, k, v, o, lse, w.scale, causal, window, stream=stream)
+        m.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.scale, causal, window, workspace=ws,
+                 stream=stream)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # warm-up (tensor maps, kernel attributes) off the capture
+        step(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(torch.cuda.current_stream())
+    for inputs in (x2, x):
+        for n in ("q", "k", "v", "do"):
+            bufs[n].copy_(inputs[n].to(dev))
+        g.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in (o, lse, dq, dk, dv)]
+        step()
+        torch.cuda.synchronize()
+        assert m.fa_device_status() == 0
+        for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), got, (o, lse, dq, dk, dv)):
+            assert torch.equal(a, b), name
